@@ -59,12 +59,12 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def tensor_peak(p: W.Problem, pk: dict, sustained: bool = True) -> float:
+def tensor_peak(p: W.Problem, pk: dict, sustained: bool = False) -> float:
     """Peak TFLOP/s of the GEMM's input type: measured bf16 x the nominal ratio
-    (i8 runs on the bf16 tensor path here, so it takes the bf16 peak).  The
-    kernels are timed inside a long run of steps in which the GPU reaches its
-    power cap, so the sustained figure is the default; the burst one is also
-    reported."""
+    (i8 runs on the bf16 tensor path here, so it takes the bf16 peak).  Each
+    kernel is timed as one launch of a few milliseconds, not inside a seconds-long
+    step, so the burst figure is the default; the sustained one (a back-to-back
+    loop under the power cap) is also reported."""
     base = pk["bf16_tflops_sustained" if sustained else "bf16_tflops"]
     return base * RATE_VS_BF16[p.ta] * (2.0 if p.sparse else 1.0)
 
@@ -227,7 +227,7 @@ def algorithmic_bytes(p: W.Problem) -> int:
     return a + b + 2 * p.M * p.N * (2 if p.tacc in ("f16", "bf16") else 4)
 
 
-def small_case(mm, dev, reps: int = 21) -> dict:
+def small_case(mm, dev, hbm_gbs: float, reps: int = 21) -> dict:
     """The smallest configuration (dense f16 128 x 128 x 256, one tile: launch- and
     latency-bound) timed per call on the device, warm (inputs in L2) and cold (L2
     flushed by writing a buffer twice its size first).  A device-side sleep ahead of
@@ -252,8 +252,10 @@ def small_case(mm, dev, reps: int = 21) -> dict:
         ts.sort()
         out[f"us_{mode}"] = round(ts[len(ts) // 2], 2)
     byts = algorithmic_bytes(p)
+    gbs = {m: byts / (out[f"us_{m}"] * 1e-6) / 1e9 for m in ("warm", "cold")}
     return {"workload": "dense_f16_128", "M": p.M, "N": p.N, "K": p.K, **out,
-            "algorithmic_bytes": byts, "gbs_warm": round(byts / (out["us_warm"] * 1e-6) / 1e9, 1),
+            "algorithmic_bytes": byts, "gbs_warm": round(gbs["warm"], 1), "gbs_cold": round(gbs["cold"], 1),
+            "frac_of_hbm_warm": round(gbs["warm"] / hbm_gbs, 5), "frac_of_hbm_cold": round(gbs["cold"] / hbm_gbs, 5),
             "tflops_warm": round(p.flops / (out["us_warm"] * 1e-6) / 1e12, 3),
             "what": "median of 21 single calls, each queued behind a device-side sleep"}
 
@@ -300,6 +302,84 @@ def record_traffic(args):
     print(json.dumps(d[f"{kernel}:{name}"]))
 
 
+NCU_PATH = os.path.join(ROOT, "profiles", "ncu.json")
+# the counters kept per GEMM kernel and workload (one ncu pass group, a few passes)
+NCU_METRICS = ("gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_write.sum",
+               "sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed",
+               "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed", "sm__cycles_elapsed.avg.per_second")
+
+
+def _ncu_launches(csv_path: str, pattern: str) -> list[dict]:
+    """Per-launch metric dictionaries of the kernels matching ``pattern`` in an ncu
+    CSV (``--csv`` output of ``--metrics``)."""
+    import csv
+    with open(csv_path) as f:
+        rows = [ln for ln in f if ln.startswith('"')]
+    launches = {}
+    for row in csv.DictReader(rows):
+        if pattern not in row["Kernel Name"]:
+            continue
+        m = launches.setdefault(row["ID"], {})
+        try:
+            m[row["Metric Name"]] = float(row["Metric Value"].replace(",", ""))
+        except ValueError:
+            pass
+    return list(launches.values())
+
+
+def record_ncu(args):
+    """Read an ncu CSV of one workload's GEMM launches (the NCU_METRICS counters)
+    and store their per-launch means, with the kernel's source digest and the
+    captured shape, in profiles/ncu.json."""
+    if not args.workloads or len(args.workloads) != 1:
+        raise SystemExit("--record-ncu needs exactly one --workloads entry")
+    name = args.workloads[0]
+    r = W.RECIPES[name]
+    M, N, K = args.shape if args.shape else (r.M, r.N, r.K)
+    prob = W.Problem(name, M, N, K, r.ta, r.tb, r.tacc, None, None, None, r.sparse, None)
+    kernel, pattern = kernel_of(prob)
+    got = [m for m in _ncu_launches(args.record_ncu, pattern) if all(k in m for k in NCU_METRICS)]
+    if not got:
+        raise SystemExit(f"no {pattern} launch with the ncu counters in {args.record_ncu}")
+    mean = {k: sum(m[k] for m in got) / len(got) for k in NCU_METRICS}
+    dur = mean["gpu__time_duration.sum"] * 1e-9
+    rd, wr = mean["dram__bytes_read.sum"], mean["dram__bytes_write.sum"]
+    try:
+        with open(NCU_PATH) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        d = {}
+    pk, _ = peaks()
+    d[f"{kernel}:{name}"] = {
+        "shape": [M, N, K], "launches": len(got), "ncu_duration_us": round(dur * 1e6, 2),
+        "sm_mhz": round(mean["sm__cycles_elapsed.avg.per_second"] / 1e6, 1),
+        "tensor_pipe_active_pct": round(mean["sm__pipe_tensor_cycles_active.avg.pct_of_peak_sustained_elapsed"], 2),
+        "dram_read": int(rd), "dram_write": int(wr), "dram_gbs": round((rd + wr) / dur / 1e9, 1),
+        "dram_frac_of_hbm": round((rd + wr) / dur / 1e9 / pk["hbm_gbs"], 4),
+        "dram_throughput_pct": round(mean["gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed"], 2),
+        "algorithmic_bytes": algorithmic_bytes(prob),
+        "tflops_under_ncu": round(prob.flops / dur / 1e12, 1),
+        "source_digest": source_digest(kernel), "csv": os.path.basename(args.record_ncu)}
+    with open(NCU_PATH, "w") as f:
+        json.dump(d, f, indent=1)
+        f.write("\n")
+    print(json.dumps(d[f"{kernel}:{name}"]))
+
+
+def recorded_ncu(kernel: str, workload: str):
+    """The committed ncu counters of this kernel on this workload, if they were
+    taken on the current kernel sources (None otherwise)."""
+    try:
+        with open(NCU_PATH) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    rec = d.get(f"{kernel}:{workload}")
+    if not rec or rec.get("source_digest") != source_digest(kernel):
+        return None
+    return {k: v for k, v in rec.items() if k not in ("source_digest", "csv")}
+
+
 def cpu_sample(problems, frac_rows: int, oracle_mod):
     """Time the oracle on every frac_rows-th row of each workload; returns
     (flops of the sample, seconds, threads, description)."""
@@ -320,6 +400,26 @@ def cpu_sample(problems, frac_rows: int, oracle_mod):
         flops += 2 * len(rows) * p.N * p.K
     desc = f"every {frac_rows}th row of each suite workload (all columns, full K)"
     return flops, secs, oracle_mod.num_threads(), desc
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
 
 
 def dist_setup(n_gpus: int):
@@ -410,7 +510,7 @@ def run_ours(args):
     def tc_kind(p):
         # the 8-bit integer GEMMs run on bf16 operands
         return ("e4m3" if p.ta in ("e4m3", "e5m2") else "bf16") + ("_sparse" if p.sparse else "")
-    small = small_case(mm, dev) if not args.shape else None
+    small = small_case(mm, dev, pk["hbm_gbs"]) if not args.shape else None
 
     def legacy_kind(p):
         if p.ta in ("i8", "u8"):
@@ -429,8 +529,11 @@ def run_ours(args):
                "types": f"{e.p.ta}x{e.p.tb}->{e.p.tacc}", "sparse": e.p.sparse,
                "ms": round(ms, 4), "gemm_ms": round(gemm_ms, 4), "tflops": round(tf, 1),
                "peak_tflops": round(peak, 1), "frac_of_peak": round(tf / peak, 4),
-               "frac_of_burst_peak": round(tf / tensor_peak(e.p, pk, sustained=False), 4)}
+               "frac_of_sustained_peak": round(tf / tensor_peak(e.p, pk, sustained=True), 4)}
         rec["frac_of_nominal_peak"] = round(tf / nominal[tc_kind(e.p)], 4)
+        # ncu counters of this GEMM's kernel (one launch, cold, serialised; taken on
+        # the shape named in the record), when captured on the current sources
+        rec["ncu"] = recorded_ncu(kernel_of(e.p)[0], e.name) if not args.shape else None
         lk = legacy_kind(e.p)
         if lk:
             rec["vs_legacy_mma_peak"] = round(tf / legacy[lk], 3)
@@ -448,9 +551,10 @@ def run_ours(args):
     roofline = {"bound": "tensor", "kernel": kernel, "workload": entries[dom].name,
                 "achieved": achieved, "peak": round(peak, 1), "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4),
-                "frac_of_burst_peak": round(achieved / tensor_peak(dp, pk, sustained=False), 4),
+                "frac_of_sustained_peak": round(achieved / tensor_peak(dp, pk, sustained=True), 4),
                 "frac_of_nominal_peak": round(achieved / nominal[tc_kind(dp)], 4),
-                "peak_source": f"{pk_src} bf16 sustained x {RATE_VS_BF16[dp.ta] * (2 if dp.sparse else 1):g} (nominal type ratio)",
+                "peak_source": f"{pk_src} bf16 burst x {RATE_VS_BF16[dp.ta] * (2 if dp.sparse else 1):g} (nominal type ratio); "
+                               "frac_of_nominal_peak: SMs x measured tcgen05 ops per clock x the maximum SM clock",
                 "traffic": recorded_traffic(kernel, entries[dom].name) if not args.shape else None,
                 "algorithmic_bytes": algorithmic_bytes(dp)}
 
@@ -587,8 +691,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu:   # the CPU baseline is an N = 1 figure
         import oracle
         f, s, thr, desc = cpu_sample([(e.name, e.p) for e in entries], args.cpu_rows, oracle)
-        cpu = {"value": round(f / s / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-               "sample": desc, "seconds": round(s, 2)}
+        cpu = {"value": round(f / s / 1e12, 6), "unit": "TFLOP/s", "cores": thr, "cpu_model": cpu_model(),
+               "kind": "oracle", "sample": desc, "seconds": round(s, 2)}
 
     if rank == 0:
         line = {"metric": "GEMM TFLOP/s per dtype, dense and 4:2-sparse, as % of GB300 tensor peak",
@@ -695,8 +799,8 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64/i64 (oracle)",
             "data": "synthetic, seeded", "config": {"workload": "suite: " + ",".join(names)},
             "impl": "reference",
-            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                             "sample": desc},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": thr, "cpu_model": cpu_model(),
+                             "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -719,9 +823,14 @@ def main():
                     help="time only the bandwidth-bound steps (compression, pruning, quantisation)")
     ap.add_argument("--record-traffic", metavar="CSV", default=None,
                     help="store the DRAM bytes per launch of one workload's GEMM from an ncu CSV; no GPU")
+    ap.add_argument("--record-ncu", metavar="CSV", default=None,
+                    help="store one workload's GEMM counters (tensor pipe, DRAM) from an ncu CSV; no GPU")
     args = ap.parse_args()
     if args.record_traffic:
         record_traffic(args)
+        return
+    if args.record_ncu:
+        record_ncu(args)
         return
     if args.aux:
         run_aux(args)

@@ -58,7 +58,7 @@
 extern "C" {
 #endif
 
-#define MMA42_ABI_VERSION 4
+#define MMA42_ABI_VERSION 5
 
 /* Element types. */
 typedef enum {
@@ -70,7 +70,7 @@ typedef enum {
   MMA_F32 = 6,  /* IEEE binary32 (C and D of float inputs) */
   MMA_I32 = 7,  /* signed 32-bit integer (C and D of 8-bit integer inputs) */
   MMA_U8 = 8    /* unsigned 8-bit integer ("RDNA3 dense WMMA builtins", section
-                   "Fragment layouts": a_neg / b_neg false reads an integer
+                   "Common parameters": a_neg / b_neg false reads an integer
                    operand as unsigned; each operand chooses on its own) */
 } mma_dtype_t;
 
@@ -114,8 +114,8 @@ enum { MMA_FLAG_CLAMP = 1 };
 
 /* mma_gemm with options.  flags = 0 is mma_gemm.  MMA_FLAG_CLAMP (8-bit integer
  * types only, else MMA_ERR_UNSUPPORTED): D = the exact C + A*B saturated to the i32
- * range instead of wrapped ("RDNA3 dense WMMA builtins", section "Fragment
- * layouts", parameter clamp; the page's "range of the input type" is read as the
+ * range instead of wrapped ("RDNA3 dense WMMA builtins", section "Common
+ * parameters", parameter clamp; the page's "range of the input type" is read as the
  * range of the i32 accumulator).  With clamp, K is cut into slices short enough
  * that each slice's product sum fits i32, and their sum with C is formed exactly
  * in 64 bits; this draws ksplit * M * N * 4 bytes of scratch when K needs more
@@ -195,10 +195,14 @@ mma_status_t sparse42_gemm(const void* vals, const uint8_t* idx, const void* B, 
  * device-wide synchronisation, a runtime that forbids allocation after
  * start-up.  It calls no allocator.
  *   Types: (F16,F16,F32), (BF16,BF16,F32), FP8 x FP8 -> F32 (i8 is rejected
- *   with MMA_ERR_UNSUPPORTED).  Other argument rules as mma_gemm.
+ *   with MMA_ERR_UNSUPPORTED).  Layout, alignment and aliasing rules as mma_gemm.
+ *   A, B, C, D and `stream` must belong to the current device (the array used
+ *   is the current device's); a D that is not device memory of the current
+ *   device returns MMA_ERR_INVALID_ARG.
  *   Limits: 2 <= ksplit <= 16, ksplit <= the number of K blocks (64 elements
  *   for 16-bit inputs, 128 for FP8), and ksplit * M * N * 4 <= 32 MiB; a call
- *   beyond them returns MMA_ERR_SHAPE and launches nothing.
+ *   beyond them returns MMA_ERR_SHAPE and launches nothing.  Unlike mma_gemm,
+ *   K == 0 is therefore rejected (MMA_ERR_SHAPE); M == 0 or N == 0 is MMA_OK.
  *   The array is shared by every call on a device and keeps the last call's
  *   contents (no part of it needs clearing: each call writes every partial it
  *   reads).  Calls whose work overlaps on the GPU race on it.
@@ -253,9 +257,35 @@ mma_status_t mma_legacy_mma_peak(int32_t kind, double* ops_per_s, void* stream);
  * that runs out is reported by mma_sync_status like the GEMMs' (ABI 4). */
 mma_status_t mma_tcgen05_peak(int32_t kind, double* ops_per_s, double* ops_per_clk_sm, void* stream);
 
-/* Test hook: when `mode` is 1, the next dense mma_gemm launch arms its first
- * pipeline stage but never issues that stage's loads, so the consumer's wait
- * runs out and the timeout path is exercised.  Resets to 0 after one launch. */
+/* Measurement helper, not part of the GEMM path: how fast TMA fills the CTA-pair
+ * kernels' pipeline ring, measured now with nothing consuming the data.  Every SM
+ * pair (at most `clusters`, 0: as many as fit) runs the pair kernels' producer
+ * loop alone: per stage, both CTAs load `nbox` boxes (box b: box_rows[b] rows of
+ * box_row_bytes[b] bytes; 64-byte rows 64-byte swizzled, 128-byte rows 128-byte
+ * swizzled, 256-byte rows unswizzled) with the pair form of the tiled TMA load,
+ * completing on the first CTA's barrier, and one thread of that CTA hands each
+ * filled stage straight back; `stages` stages form the ring.  The source is a
+ * `src_bytes` device buffer drawn from the library's pool (one quarter per box;
+ * a buffer that fits in L2 measures the L2 -> shared memory feed).
+ * *bytes_per_clk_sm receives the bytes one SM receives per SM clock cycle, and
+ * *rows_per_clk_sm (nullable) the box rows, both counted on the SMs (clock64) over
+ * about 10 ms after a warm-up launch.  Limits: 1 <= nbox <= 4, rows a multiple of
+ * 8 in [8, 256], row bytes 64, 128 or 256, every box a multiple of 1024 bytes,
+ * stages >= 2 and the ring within 227
+ * KB of shared memory, src_bytes / 4 at least 512 rows of 16384 bytes; otherwise
+ * MMA_ERR_INVALID_ARG or MMA_ERR_SHAPE.  Waits for the stream (ABI 5). */
+mma_status_t mma_tma_feed_probe(int32_t nbox, const int32_t* box_rows, const int32_t* box_row_bytes, int32_t stages,
+                                int32_t clusters, int64_t src_bytes, double* bytes_per_clk_sm,
+                                double* rows_per_clk_sm, void* stream);
+
+/* Test hook.  `mode` 1: the next launch of the one-SM dense kernel arms its first
+ * pipeline stage but never issues that stage's loads.  `mode` 2: the next launch
+ * of a CTA-pair kernel (dense mma_gemm on the pair kernel, or sparse42_gemm) has
+ * its first cluster arm its first stage for 16 bytes more than that stage's loads
+ * bring (every load is issued and lands).  Either way that stage never completes,
+ * the MMA thread's bounded wait runs out and the timeout path is exercised
+ * (MMA_ERR_TIMEOUT from mma_sync_status).  The hook disarms itself when a launch
+ * of its kind takes it; 0 disarms it. */
 void mma_debug_inject(int32_t mode);
 
 #ifdef __cplusplus

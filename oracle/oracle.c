@@ -208,7 +208,7 @@ int oracle_gemm_f64(const void* A, int ta, const void* B, int tb, const float* C
 
 /*
  * Value of an 8-bit integer element.  "RDNA3 dense WMMA builtins", section
- * "Fragment layouts" (parameters a_neg / b_neg): integer operands are read as
+ * "Common parameters" (parameters a_neg / b_neg): integer operands are read as
  * signed or unsigned per operand; ORC_I8 is the signed reading, ORC_U8 the
  * unsigned one.
  */

@@ -81,6 +81,13 @@ std::atomic<unsigned long long> g_wait_ns{2000000000ull};
 std::atomic<int> g_inject{0};
 std::atomic<unsigned long long> g_launches{0};
 
+// The armed test hook if it is `mode` (then disarmed), else 0: mode 1 is taken by
+// the next one-SM dense launch, mode 2 by the next CTA-pair launch (dense or sparse).
+int take_inject(int mode) {
+  int want = mode;
+  return g_inject.compare_exchange_strong(want, 0) ? mode : 0;
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -254,7 +261,7 @@ mma_status_t run_gemm(const DeviceState& ds, Variant v, const void* A, int64_t a
   a.err = ds.err;
   a.wait_ns = g_wait_ns.load();
   a.inject = (v == V_DENSE_F16 || v == V_DENSE_F8 || v == V_DENSE_F16_N128 || v == V_DENSE_F8_N128)
-                 ? g_inject.exchange(0)
+                 ? take_inject(1)
                  : 0;
   const int64_t units = tiles * a.ksplit;
   p.grid = static_cast<int>(std::min<int64_t>(units, ds.num_sms));
@@ -340,7 +347,7 @@ mma_status_t run_sparse(const DeviceState& ds, const void* vals, const uint8_t* 
   a.idesc = make_idesc(fmt_code(t.a), fmt_code(t.b), si.bn, true, 2 * si.bm);
   a.err = ds.err;
   a.wait_ns = g_wait_ns.load();
-  a.inject = 0;
+  a.inject = take_inject(2);
   const int64_t units = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
   const int grid = static_cast<int>(std::min<int64_t>(units, max_clusters)) * 2;
 
@@ -508,7 +515,7 @@ mma_status_t run_pair(const DeviceState& ds, Variant v, const void* A, int a_byt
   a.idesc = make_idesc(a_fmt, b_fmt, vi.bn, false, 2 * vi.bm);
   a.err = ds.err;
   a.wait_ns = g_wait_ns.load();
-  a.inject = 0;
+  a.inject = take_inject(2);
   const int64_t units = a.tail_split > 1 ? a.tail_from + tail * a.tail_split : blocks * a.ksplit;
   const int grid = static_cast<int>(std::min<int64_t>(units, max_clusters)) * 2;
 
@@ -751,6 +758,101 @@ mma_status_t mma_tcgen05_peak(int32_t kind, double* ops_per_s, double* ops_per_c
   cudaFreeAsync(cycles, s);
   if (e0) cudaEventDestroy(e0);
   if (e1) cudaEventDestroy(e1);
+  return from_cuda(e);
+}
+
+mma_status_t mma_tma_feed_probe(int32_t nbox, const int32_t* box_rows, const int32_t* box_row_bytes, int32_t stages,
+                                int32_t clusters, int64_t src_bytes, double* bytes_per_clk_sm, double* rows_per_clk_sm,
+                                void* stream) {
+  if (nbox < 1 || nbox > 4 || !box_rows || !box_row_bytes || !bytes_per_clk_sm || clusters < 0 || stages < 2)
+    return MMA_ERR_INVALID_ARG;
+  FeedProbe p = {};
+  p.nbox = nbox;
+  int off = 0, rows = 0;
+  for (int b = 0; b < nbox; ++b) {
+    const int r = box_rows[b], rb = box_row_bytes[b];
+    if ((rb != 64 && rb != 128 && rb != 256) || r < 8 || r > 256 || r % 8 != 0 || (r * rb) % 1024 != 0)
+      return MMA_ERR_INVALID_ARG;
+    p.rows[b] = r;
+    p.row_bytes[b] = rb;
+    p.smem_off[b] = off;   // r * rb is a multiple of 1024: every box keeps the swizzle alignment
+    off += r * rb;
+    rows += r;
+  }
+  p.stages = stages;
+  p.stage_bytes = off;
+  const int pitch = feed_probe_row_pitch();
+  const int64_t quarter = src_bytes / 4;
+  if (src_bytes < 0 || quarter / pitch < 512 || quarter / pitch > (int64_t(1) << 30)) return MMA_ERR_SHAPE;
+  p.height = static_cast<int>(quarter / pitch);
+  const int smem = stages * off + 1024 + 256;
+  if (smem > 232448) return MMA_ERR_SHAPE;
+  DeviceState* ds = nullptr;
+  mma_status_t st = device_state(&ds);
+  if (st != MMA_OK) return st;
+  const int fit = feed_probe_max_clusters(smem);
+  if (fit <= 0) return MMA_ERR_CUDA;
+  const int n = clusters == 0 ? fit : std::min(clusters, fit);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* src = nullptr;
+  unsigned long long* cycles = nullptr;
+  if (cudaMallocFromPoolAsync(&src, static_cast<size_t>(src_bytes), ds->pool, s) != cudaSuccess) return MMA_ERR_CUDA;
+  if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&cycles), static_cast<size_t>(n) * 8, ds->pool, s) !=
+      cudaSuccess) {
+    cudaFreeAsync(src, s);
+    return MMA_ERR_CUDA;
+  }
+  CUtensorMap maps[4];
+  bool ok = true;
+  for (int b = 0; b < 4 && ok; ++b) {
+    const int bb = b < nbox ? b : 0;
+    const uint64_t dims[2] = {static_cast<uint64_t>(pitch), static_cast<uint64_t>(p.height)};
+    const uint64_t str[1] = {static_cast<uint64_t>(pitch)};
+    const uint32_t box[2] = {static_cast<uint32_t>(p.row_bytes[bb]), static_cast<uint32_t>(p.rows[bb])};
+    const CUtensorMapSwizzle swz = p.row_bytes[bb] == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                                   : p.row_bytes[bb] == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                           : CU_TENSOR_MAP_SWIZZLE_NONE;
+    ok = encode(&maps[b], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, static_cast<uint8_t*>(src) + bb * quarter, dims, str, box,
+                swz);
+  }
+  cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
+  // a first launch warms L2 and sizes the timed one at about 10 ms
+  p.iters = 1024;
+  std::vector<unsigned long long> cyc(static_cast<size_t>(n));
+  for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
+    e = launch_feed_probe(p, maps, n, g_wait_ns.load(), ds->err, cycles, s);
+    if (e == cudaSuccess) g_launches.fetch_add(1);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(cyc.data(), cycles, cyc.size() * 8, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && pass == 0) {
+      double mean = 0.0;
+      for (unsigned long long c : cyc) mean += static_cast<double>(c);
+      mean /= static_cast<double>(cyc.size());
+      const double per_stage = mean / (p.iters - feed_probe_warm_stages());
+      // about 2e7 cycles (10 ms at 2 GHz)
+      p.iters = static_cast<int>(std::max(1024.0, std::min(1e6, 2e7 / std::max(per_stage, 1.0))));
+    }
+  }
+  if (e == cudaSuccess) {
+    double mean = 0.0;
+    int counted = 0;
+    for (unsigned long long c : cyc)
+      if (c) {
+        mean += static_cast<double>(c);
+        ++counted;
+      }
+    if (counted == 0) {
+      e = cudaErrorUnknown;
+    } else {
+      mean /= counted;
+      const double stages_timed = p.iters - feed_probe_warm_stages();
+      *bytes_per_clk_sm = p.stage_bytes * stages_timed / mean;   // each SM fills its own stage_bytes per stage
+      if (rows_per_clk_sm) *rows_per_clk_sm = rows * stages_timed / mean;
+    }
+  }
+  cudaFreeAsync(cycles, s);
+  cudaFreeAsync(src, s);
+  if (!ok) return MMA_ERR_CUDA;
   return from_cuda(e);
 }
 

@@ -188,6 +188,7 @@ __global__ void __launch_bounds__(PairCfg<KIND, INTACC>::THREADS, 1)
         uint32_t issued_phase[S];
         for (int s = 0; s < S; ++s) issued[s] = false;
         bool ok = true;
+        bool first = true;
         for (int u = cid; u < units && ok; u += ncl) {
           const WorkUnit wu = unit_of(u, tiles, args);
           int mt, nt;
@@ -198,7 +199,12 @@ __global__ void __launch_bounds__(PairCfg<KIND, INTACC>::THREADS, 1)
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!wait_phase(empty_bar(stage), phase ^ 1u, args, abort_flag)) { ok = false; break; }
             const uint32_t fb = mapa_shared(full_bar(stage), 0);
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * Cfg::STAGE_BYTES);
+            // test hook (mma_debug_inject(2)): cluster 0 arms its first stage for 16 bytes
+            // more than its loads bring, so that stage never completes and the MMA
+            // thread's bounded wait runs out; every load is still issued and lands
+            const uint32_t extra = (args.inject == 2 && cid == 0 && first) ? 16u : 0u;
+            first = false;
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * Cfg::STAGE_BYTES + extra);
             const uint32_t sa = sbase + stage * Cfg::STAGE_BYTES;
             const uint32_t sb = sa + Cfg::A_BYTES;
             tma_load_2d_pair(sa, &tmA, kb * Cfg::BK, m0, fb);

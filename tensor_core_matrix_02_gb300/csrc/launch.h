@@ -130,6 +130,23 @@ int tc_peak_max_clusters(int kind);
 cudaError_t launch_tc_peak(int kind, int64_t iters, uint32_t idesc, uint64_t wait_ns, unsigned long long* cycles,
                            int* err, int clusters, cudaStream_t stream);
 
+// TMA feed probe (feed_probe.cu): the producer loop of the CTA-pair kernels alone.
+// Up to four boxes per stage (rows x row_bytes each, placed at smem_off within the
+// stage), `stages` stages of stage_bytes, iters stages per CTA; the maps are 2-D
+// byte matrices of feed_probe_row_pitch()-byte rows and `height` rows, one per box.
+// cycles[cluster] receives the SM cycles of the stages after the first
+// feed_probe_warm_stages() (0 if a wait ran out).
+struct FeedProbe {
+  int nbox;
+  int rows[4], row_bytes[4], smem_off[4];
+  int stages, stage_bytes, iters, height;
+};
+int feed_probe_max_clusters(int smem_bytes);
+int feed_probe_row_pitch();
+int feed_probe_warm_stages();
+cudaError_t launch_feed_probe(const FeedProbe& p, const CUtensorMap* maps, int clusters, uint64_t wait_ns, int* err,
+                              unsigned long long* cycles, cudaStream_t stream);
+
 // Tail split of the CTA-pair kernel: D = C + sum_s P[s] over the tail tiles only.
 // P is compact: tail_split x (T * tile_rows) x tile_cols, tile t of the tail being
 // raster tile tail_from + t of the GEMM described by g (tiles_m, tiles_n, group_m).

@@ -14,8 +14,10 @@
 //
 // Contract (also in include/mma42.h):
 //  * ksplit * M * N * 4 bytes must fit in kScratchBytes (32 MiB); larger requests,
-//    ksplit outside [2, 16] and ksplit above the number of K blocks are rejected
-//    with MMA_ERR_SHAPE before anything is launched.
+//    ksplit outside [2, 16] and ksplit above the number of K blocks (so also
+//    K == 0) are rejected with MMA_ERR_SHAPE before anything is launched.
+//  * A, B, C, D and the stream belong to the current device; a D that is not
+//    device memory of the current device is rejected with MMA_ERR_INVALID_ARG.
 //  * Every call on a device uses the same array and it keeps the last call's
 //    contents.  Nothing in it needs to start at zero: each call writes every
 //    partial element it later reads.  Calls whose work overlaps on the GPU (two
@@ -75,6 +77,17 @@ mma_status_t noalloc_device(NoAllocDevice** out) {
   return MMA_OK;
 }
 
+// p is device memory of the current device (a query; allocates nothing)
+bool on_current_device(const void* p) {
+  int dev = 0;
+  cudaPointerAttributes at;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();   // clear a sticky query error
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
 bool float_types(const mma_dtypes_t& t) {
   if (t.acc != MMA_F32) return false;
   if (t.a == MMA_F16 && t.b == MMA_F16) return true;
@@ -93,7 +106,9 @@ extern "C" mma_status_t mma_gemm_splitk_noalloc(const void* A, const void* B, co
   mma_status_t st = host::check_gemm_args(A, K * ea, M * K * ea, B, C, D, M, N, K, eb, 4);
   if (st != MMA_OK || M == 0 || N == 0) return st;
   const bool f8 = host::fp8_type(t.a);
-  const Variant v = f8 ? V_DENSE_F8 : V_DENSE_F16;
+  // outputs at most 128 wide take 128-column blocks, as in mma_gemm: no MMA, B
+  // staging or epilogue work on columns past N
+  const Variant v = N <= 128 ? (f8 ? V_DENSE_F8_N128 : V_DENSE_F16_N128) : (f8 ? V_DENSE_F8 : V_DENSE_F16);
   const VariantInfo vi = variant_info(v);
   const int64_t kblocks = (K + vi.bkl - 1) / vi.bkl;
   if (ksplit < 2 || ksplit > 16 || ksplit > kblocks) return MMA_ERR_SHAPE;
@@ -101,6 +116,9 @@ extern "C" mma_status_t mma_gemm_splitk_noalloc(const void* A, const void* B, co
 
   NoAllocDevice* dev = nullptr;
   if ((st = noalloc_device(&dev)) != MMA_OK) return st;
+  // the array lives on the current device: an output on another device would have
+  // the kernel read and write the wrong GPU's memory
+  if (!on_current_device(D)) return MMA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   GemmArgs a;

@@ -29,7 +29,8 @@ STATUS = {0: "MMA_OK", 1: "MMA_ERR_INVALID_ARG", 2: "MMA_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ("mma_gemm", "mma_gemm_ex", "sparse42_compress", "sparse42_prune", "sparse42_gemm", "mma_quantize",
            "sparse42_quantize_prune", "mma_sync_status",
            "mma_status_string", "mma_abi_version", "mma_set_wait_limit_ns", "mma_debug_inject",
-           "mma_launch_count", "mma_gemm_splitk_noalloc", "mma_legacy_mma_peak", "mma_tcgen05_peak")
+           "mma_launch_count", "mma_gemm_splitk_noalloc", "mma_legacy_mma_peak", "mma_tcgen05_peak",
+           "mma_tma_feed_probe")
 
 
 class MmaError(RuntimeError):
@@ -94,6 +95,9 @@ def load_library(path: str | None = None):
         lib.mma_legacy_mma_peak.restype = i32
         lib.mma_tcgen05_peak.argtypes = [i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double), vp]
         lib.mma_tcgen05_peak.restype = i32
+        pi32, pd = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_double)
+        lib.mma_tma_feed_probe.argtypes = [i32, pi32, pi32, i32, i32, i64, pd, pd, vp]
+        lib.mma_tma_feed_probe.restype = i32
         if path is None:
             _lib = lib
         return lib
@@ -166,6 +170,22 @@ def mma_tcgen05_peak(kind: str, stream=None) -> tuple[float, float]:
     _check(load_library().mma_tcgen05_peak(TCGEN05_KINDS[kind], ctypes.byref(ops), ctypes.byref(per_clk),
                                            _stream(stream)), "mma_tcgen05_peak")
     return ops.value, per_clk.value
+
+
+def mma_tma_feed_probe(boxes, stages: int, clusters: int = 0, src_bytes: int = 64 << 20,
+                       stream=None) -> tuple[float, float]:
+    """TMA fill rate of the CTA-pair kernels' pipeline ring with nothing consuming
+    it, measured now on the current device.  ``boxes``: up to four (rows, row
+    bytes) boxes per stage; ``stages`` in the ring; ``clusters`` SM pairs (0: all
+    that fit); ``src_bytes`` of source (64 MB stays in L2).  Returns (bytes, box
+    rows) per SM clock cycle per SM."""
+    n = len(boxes)
+    rows = (ctypes.c_int32 * 4)(*[int(r) for r, _ in boxes], *([0] * (4 - n)))
+    rb = (ctypes.c_int32 * 4)(*[int(b) for _, b in boxes], *([0] * (4 - n)))
+    byts, rws = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    _check(load_library().mma_tma_feed_probe(n, rows, rb, stages, clusters, src_bytes, ctypes.byref(byts),
+                                             ctypes.byref(rws), _stream(stream)), "mma_tma_feed_probe")
+    return byts.value, rws.value
 
 
 MMA_FLAG_CLAMP = 1

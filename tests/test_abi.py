@@ -51,7 +51,7 @@ def test_library_has_no_runtime_dependency_beyond_libc(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.mma_abi_version() == 4
+    assert lib.mma_abi_version() == 5
     for code, name in mma42.STATUS.items():
         assert lib.mma_status_string(code).decode().startswith(name)
     assert b"unknown" in lib.mma_status_string(99)
@@ -190,3 +190,19 @@ def test_tcgen05_peak_rejects_bad_arguments(lib):
     assert lib.mma_tcgen05_peak(4, ctypes.byref(out), None, None) == 1
     assert lib.mma_tcgen05_peak(-1, ctypes.byref(out), None, None) == 1
     assert lib.mma_tcgen05_peak(0, None, None, None) == 1
+
+
+def test_feed_probe_rejects_bad_arguments(lib):
+    """Checked on the host before any CUDA call."""
+    out = ctypes.c_double(0.0)
+    I4 = ctypes.c_int32 * 4
+    ok_rows, ok_bytes = I4(128, 64, 0, 0), I4(64, 128, 0, 0)
+    assert lib.mma_tma_feed_probe(0, ok_rows, ok_bytes, 4, 0, 64 << 20, ctypes.byref(out), None, None) == 1
+    assert lib.mma_tma_feed_probe(5, ok_rows, ok_bytes, 4, 0, 64 << 20, ctypes.byref(out), None, None) == 1
+    assert lib.mma_tma_feed_probe(2, I4(100, 64, 0, 0), ok_bytes, 4, 0, 64 << 20, ctypes.byref(out), None, None) == 1
+    assert lib.mma_tma_feed_probe(2, I4(8, 64, 0, 0), ok_bytes, 4, 0, 64 << 20, ctypes.byref(out), None, None) == 1
+    assert lib.mma_tma_feed_probe(2, ok_rows, I4(32, 128, 0, 0), 4, 0, 64 << 20, ctypes.byref(out), None, None) == 1
+    assert lib.mma_tma_feed_probe(2, ok_rows, ok_bytes, 1, 0, 64 << 20, ctypes.byref(out), None, None) == 1
+    assert lib.mma_tma_feed_probe(2, ok_rows, ok_bytes, 4, 0, 64 << 20, None, None, None) == 1
+    assert lib.mma_tma_feed_probe(2, ok_rows, ok_bytes, 4, 0, 1 << 20, ctypes.byref(out), None, None) == 3
+    assert lib.mma_tma_feed_probe(2, ok_rows, ok_bytes, 16, 0, 64 << 20, ctypes.byref(out), None, None) == 3

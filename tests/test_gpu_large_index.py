@@ -18,7 +18,7 @@ import torch
 from tensor_core_matrix_02_gb300 import mma42
 from tensor_core_matrix_02_gb300 import workloads as W
 
-from gpu_helpers import assert_matches, poisoned_like, rel_frobenius
+from gpu_helpers import assert_half_close, assert_matches, half_reference, poisoned_like, ref_dense, ref_sparse
 
 pytestmark = pytest.mark.gpu
 
@@ -60,8 +60,8 @@ def test_dense_output_past_2_31_elements(oracle, monkeypatch, kind, kernel):
     assert mma42.mma_sync_status() == 0
     rows = boundary_rows(DM, DN, 4, seed=DM)
     sel = torch.tensor(rows, device="cuda")
-    ref = oracle.gemm(W.bits(p.A[sel].cpu()), p.ta, W.bits(p.B.cpu()), p.tb, p.C[sel].cpu().numpy())
-    assert_matches(D[sel], ref, p.ta, f"{kind} {kernel} {DM}x{DN}x{DK} rows {rows}")
+    ref = ref_dense(oracle, W.bits(p.A[sel].cpu()), p.ta, W.bits(p.B.cpu()), p.tb, p.C[sel].cpu().numpy())
+    assert_matches(D[sel], ref, p.ta, f"{kind} {kernel} {DM}x{DN}x{DK} rows {rows}", tile=(1, 32))
 
 
 def test_dense_half_output_past_2_31_elements(oracle):
@@ -75,12 +75,8 @@ def test_dense_half_output_past_2_31_elements(oracle):
     assert mma42.mma_sync_status() == 0
     rows = boundary_rows(DM, DN, 2, seed=DN)
     sel = torch.tensor(rows, device="cuda")
-    ref = oracle.gemm(W.bits(p.A[sel].cpu()), "f16", W.bits(p.B.cpu()), "f16", C[sel].cpu().to(torch.float32).numpy())
-    q = oracle.quantize(ref.astype(np.float32), "f16")
-    want = torch.from_numpy(q.view(np.int16)).view(torch.float16).to(torch.float64).numpy()
-    got = D[sel].cpu().to(torch.float64).numpy()
-    assert np.isfinite(got).all()
-    assert rel_frobenius(got, want) <= 1e-3
+    rp = W.Problem(p.name, len(rows), p.N, p.K, p.ta, p.tb, "f16", p.A[sel], p.B, None, None, None)
+    assert_half_close(D[sel], half_reference(oracle, rp, C[sel], "f16"), f"f16 out rows {rows}", tile=(1, 32))
 
 
 SPARSE = {"f16": ("sparse_f16_random", None, None), "e4m3xe5m2": ("sparse_e4m3_e5m2", None, None),
@@ -104,8 +100,8 @@ def test_sparse_operand_past_2_31_elements(oracle, kind):
     assert viol == 0
     assert np.array_equal(W.bits(vals[sel].cpu()), ov), f"{kind}: compressed values differ on rows {rows}"
     assert np.array_equal(idx[sel].cpu().numpy(), oi), f"{kind}: index differs on rows {rows}"
-    ref = oracle.sparse_gemm(ov, oi, p.ta, W.bits(p.B.cpu()), p.tb, p.C[sel].cpu().numpy(), SK)
-    assert_matches(D[sel], ref, p.ta, f"{kind} sparse {SM}x{SN}x{SK} rows {rows}")
+    ref = ref_sparse(oracle, ov, oi, p.ta, W.bits(p.B.cpu()), p.tb, p.C[sel].cpu().numpy(), SK)
+    assert_matches(D[sel], ref, p.ta, f"{kind} sparse {SM}x{SN}x{SK} rows {rows}", tile=(1, 32))
     # pruning a 4:2 matrix keeps exactly its non-zeros: the same compressed form
     pv, pi = mma42.sparse42_prune(p.A)
     assert mma42.mma_sync_status() == 0

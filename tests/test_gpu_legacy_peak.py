@@ -53,3 +53,19 @@ def test_gemm_stays_below_the_tcgen05_ceiling():
     peak, _ = mma42.mma_tcgen05_peak("bf16")
     assert mma42.mma_sync_status() == 0
     assert 0 < gemm < 1.15 * peak, (gemm, peak)
+
+
+@pytest.mark.parametrize("boxes,stages", [
+    ([(128, 64), (8, 256), (64, 128), (64, 128)], 7),     # the 4:2 f16 kernel's stage
+    ([(128, 128), (64, 128), (64, 128)], 6),              # the dense bf16 kernel's stage
+    ([(128, 128)], 4),
+])
+def test_tma_feed_probe_measures(boxes, stages):
+    """The TMA fill rate of a pipeline ring: positive, and below what one SM's
+    shared memory could take in a clock (a rate far above it would mean the loads
+    were not waited for)."""
+    byts, rows = mma42.mma_tma_feed_probe(boxes, stages)
+    assert mma42.mma_sync_status() == 0
+    assert math.isfinite(byts) and 1.0 < byts < 1024.0, byts
+    per_row = sum(r * b for r, b in boxes) / sum(r for r, _ in boxes)
+    assert abs(rows * per_row - byts) <= 1e-6 * byts

@@ -12,7 +12,8 @@ import torch
 from tensor_core_matrix_02_gb300 import mma42
 from tensor_core_matrix_02_gb300 import workloads as W
 
-from gpu_helpers import TOL, assert_matches, gpu_dense, oracle_dense, poisoned_like, rel_frobenius, wrap_i32
+from gpu_helpers import (TOL, assert_half_close, assert_matches, gpu_dense, half_reference, oracle_dense, poisoned_like,
+                         ref_sparse, rel_frobenius, wrap_i32)
 
 pytestmark = pytest.mark.gpu
 
@@ -217,19 +218,6 @@ def half_case(kind, M, N, K):
     p = W.make(HALF[kind], M=M, N=N, K=K)
     C = p.C.to(W.TORCH_DTYPE[kind])
     return p, C
-
-
-def half_reference(oracle, p, C, kind):
-    ref = oracle.gemm(W.bits(p.A), p.ta, W.bits(p.B), p.tb, C.to(torch.float32).numpy())
-    q = oracle.quantize(ref.astype(np.float32), kind)
-    return torch.from_numpy(q.view(np.int16)).view(W.TORCH_DTYPE[kind]).to(torch.float64).numpy()
-
-
-def assert_half_close(D, want, what):
-    got = D.cpu().to(torch.float64).numpy()
-    assert np.isfinite(got).all(), f"{what}: non-finite output"
-    err = rel_frobenius(got, want)
-    assert err <= 1e-3, f"{what}: relative Frobenius error {err:.3e}"
 
 
 @pytest.mark.parametrize("kind", ["f16", "bf16"])
@@ -497,7 +485,7 @@ def test_prune_then_sparse_gemm_matches_oracle(oracle, name):
     D = mma42.sparse42_gemm(vals, idx, p.B.cuda(), p.C.cuda(), poisoned_like(p.C.cuda()))
     assert mma42.mma_sync_status() == 0
     ov, oi, _ = oracle.prune(W.bits(p.A), p.ta)
-    ref = oracle.sparse_gemm(ov, oi, p.ta, W.bits(p.B), p.tb, p.C.numpy(), p.K)
+    ref = ref_sparse(oracle, ov, oi, p.ta, W.bits(p.B), p.tb, p.C.numpy(), p.K)
     assert_matches(D, ref, p.ta, f"prune + sparse {name}")
 
 
@@ -583,7 +571,7 @@ def test_sparse_matches_oracle(oracle, kind, M, N, K):
     D = mma42.sparse42_gemm(vals, idx, B, C, poisoned_like(C))
     assert mma42.mma_sync_status() == 0
     ov, oi, _ = oracle.compress(W.bits(p.A), p.ta)
-    ref = oracle.sparse_gemm(ov, oi, p.ta, W.bits(p.B), p.tb, p.C.numpy(), K)
+    ref = ref_sparse(oracle, ov, oi, p.ta, W.bits(p.B), p.tb, p.C.numpy(), K)
     assert_matches(D, ref, p.ta, f"sparse {kind} {M}x{N}x{K}")
 
 

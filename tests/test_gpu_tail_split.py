@@ -15,7 +15,7 @@ import torch
 from tensor_core_matrix_02_gb300 import mma42
 from tensor_core_matrix_02_gb300 import workloads as W
 
-from gpu_helpers import assert_matches, gpu_dense, oracle_dense, rel_frobenius
+from gpu_helpers import assert_half_close, assert_matches, gpu_dense, half_reference, oracle_dense, rel_frobenius
 
 pytestmark = pytest.mark.gpu
 
@@ -61,12 +61,7 @@ def test_forced_tail_split_half_outputs(oracle, pair, kind):
     C = p.C.to(W.TORCH_DTYPE[kind])
     D = mma42.mma_gemm(p.A.cuda(), p.B.cuda(), C.cuda(), torch.full_like(C.cuda(), float("nan")))
     assert mma42.mma_sync_status() == 0
-    ref = oracle.gemm(W.bits(p.A), p.ta, W.bits(p.B), p.tb, C.to(torch.float32).numpy())
-    q = oracle.quantize(ref.astype(np.float32), kind)
-    want = torch.from_numpy(q.view(np.int16)).view(W.TORCH_DTYPE[kind]).to(torch.float64).numpy()
-    got = D.cpu().to(torch.float64).numpy()
-    assert np.isfinite(got).all()
-    assert rel_frobenius(got, want) <= 1e-3
+    assert_half_close(D, half_reference(oracle, p, C, kind), f"{kind} out, tail split")
 
 
 def test_tail_split_is_deterministic(pair):

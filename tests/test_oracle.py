@@ -172,7 +172,7 @@ def test_dense_i8_extreme_values_exact(oracle):
                                          ("i8", -1, "u8", 1)])
 def test_dense_8bit_signedness_closed_forms(oracle, ta, va, tb, vb):
     """Constant matrices: D = C + K * a * b, with each operand read as its own
-    type ("RDNA3 dense WMMA builtins", section "Fragment layouts", a_neg/b_neg)."""
+    type ("RDNA3 dense WMMA builtins", section "Common parameters", a_neg/b_neg)."""
     M, N, K = 3, 4, 640
     A = torch.full((M, K), va, dtype=W.TORCH_DTYPE[ta])
     B = torch.full((K, N), vb, dtype=W.TORCH_DTYPE[tb])
