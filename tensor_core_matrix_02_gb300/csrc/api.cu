@@ -337,7 +337,7 @@ mma_status_t run_sparse(const DeviceState& ds, const void* vals, const uint8_t* 
   a.K = static_cast<int>(K);
   a.tiles_m = static_cast<int>((M + 2 * si.bm - 1) / (2 * si.bm));   // 256-row blocks of a CTA pair
   a.tiles_n = static_cast<int>((N + si.bn - 1) / si.bn);
-  a.kblocks = static_cast<int>(K / si.bkl);
+  a.kblocks = static_cast<int>((K + si.bkl - 1) / si.bkl);   // an FP8 K of 128 mod 256 ends on half a stage
   a.ksplit = 1;
   a.chunk_kb = intacc ? std::max(1, int_chunk / si.bkl) : 0;
   a.c = C;
@@ -351,13 +351,17 @@ mma_status_t run_sparse(const DeviceState& ds, const void* vals, const uint8_t* 
   const int64_t units = static_cast<int64_t>(a.tiles_m) * a.tiles_n;
   const int grid = static_cast<int>(std::min<int64_t>(units, max_clusters)) * 2;
 
-  // the index in the tensor cores' layout (pool scratch, 16 bytes per row per MMA)
-  const int64_t slots = (K / si.bkl) * si.meta_slots;
-  const int64_t rows16 = (M + 15) / 16 * 16;
+  // the index in the tensor cores' layout (pool scratch, 8 bytes per row per 64
+  // logical K, over whole stages and whole 256-row blocks, which the kernel's index
+  // writers read without bounds checks)
+  const int64_t slots = static_cast<int64_t>(a.kblocks) * si.meta_slots;
+  const int64_t rows = static_cast<int64_t>(a.tiles_m) * 2 * si.bm;
   void* native = nullptr;
-  if (cudaMallocFromPoolAsync(&native, static_cast<size_t>(slots * rows16 * 16), ds.pool, stream) != cudaSuccess)
+  if (cudaMallocFromPoolAsync(&native, static_cast<size_t>(slots * rows * 8), ds.pool, stream) != cudaSuccess)
     return MMA_ERR_CUDA;
-  cudaError_t e = launch_meta_native(idx, native, M, K, f16, si.bkl, si.mmas, ds.num_sms, stream);
+  cudaError_t e = launch_meta_native(idx, native, M, K, f16, rows, slots, ds.num_sms, stream);
+  a.meta = native;
+  a.meta_rows = rows;
   if (e == cudaSuccess) g_launches.fetch_add(1);
 
   TensorMaps m;
@@ -366,29 +370,33 @@ mma_status_t run_sparse(const DeviceState& ds, const void* vals, const uint8_t* 
     const uint64_t dims[2] = {static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M)};
     const uint64_t str[1] = {static_cast<uint64_t>(K / 2) * ea};
     const uint32_t box[2] = {static_cast<uint32_t>(si.bka), static_cast<uint32_t>(si.bm)};
-    ok = encode(&m.a, raw_type(ea), 2, vals, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B);
+    ok = encode(&m.a, raw_type(ea), 2, vals, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
   }
   if (ok) {
     const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K)};
     const uint64_t str[1] = {static_cast<uint64_t>(N) * eb};
     const uint32_t box[2] = {static_cast<uint32_t>(si.b_atom_n), static_cast<uint32_t>(si.b_rows_per_cta)};
-    ok = encode(&m.b, raw_type(eb), 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (si.b_chunks == 2 && N % si.b_atom_n == 0) {
+      // B as (b_atom_n columns, K rows, N / b_atom_n chunks): the strides need not grow
+      // with the dimension, and one box brings both of a stage's 64-column chunks
+      const uint64_t d3[3] = {static_cast<uint64_t>(si.b_atom_n), static_cast<uint64_t>(K),
+                              static_cast<uint64_t>(N / si.b_atom_n)};
+      const uint64_t s3[2] = {static_cast<uint64_t>(N) * eb, static_cast<uint64_t>(si.b_atom_n) * eb};
+      const uint32_t b3[3] = {static_cast<uint32_t>(si.b_atom_n), static_cast<uint32_t>(si.b_rows_per_cta), 2u};
+      ok = encode(&m.b, raw_type(eb), 3, B, d3, s3, b3, CU_TENSOR_MAP_SWIZZLE_128B);
+      a.b_chunks_3d = 1;
+    } else {
+      ok = encode(&m.b, raw_type(eb), 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
   }
   if (ok) {
-    // the native index seen as 256-byte rows (16 TMEM lanes x 16 bytes): one box row
-    // per 16 lanes keeps the TMA request count low; shared memory receives the same
-    // 128 x 16-byte tile per MMA
-    const uint64_t dims[3] = {256u, static_cast<uint64_t>(rows16 / 16), static_cast<uint64_t>(slots)};
-    const uint64_t str[2] = {256u, static_cast<uint64_t>(rows16) * 16};
-    const uint32_t box[3] = {256u, static_cast<uint32_t>(si.bm / 16), static_cast<uint32_t>(si.meta_slots)};
-    ok = encode(&m.meta, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, native, dims, str, box, CU_TENSOR_MAP_SWIZZLE_NONE);
-  }
-  if (ok) {
+    // 32 rows x epi_cols f32 boxes: 128-byte rows 128-byte swizzled, 64-byte rows 64-byte
     const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
     const uint64_t str[1] = {static_cast<uint64_t>(N) * 4};
-    const uint32_t box[2] = {32u, 32u};
-    ok = encode(&m.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) &&
-         encode(&m.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, D, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint32_t box[2] = {static_cast<uint32_t>(si.epi_cols), 32u};
+    const CUtensorMapSwizzle swz = si.epi_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    ok = encode(&m.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, str, box, swz) &&
+         encode(&m.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, D, dims, str, box, swz);
   }
   m.p = m.d;
   if (ok) {

@@ -285,21 +285,24 @@ __global__ void __launch_bounds__(256) int8_colsum_kernel(const uint32_t* __rest
 
 // See launch_meta_native.  Both layouts are built from 8-byte chunks of the row-major
 // index: chunk (r, z) is bytes [8z, 8z + 8) of row r (K/8 bytes a row), the index of
-// one 64-element K slice (f16: one stage, both MMAs; FP8: one MMA).  A block loads a
+// one 64-element K slice (f16: two 32-K MMAs; FP8: one 64-K MMA).  A block loads a
 // 32-row x 32-chunk tile with loads along the rows, then writes the tensor-core layout
 // with stores along r.  kind::f16 (one entry per stage): word kk of the entry of lane r
 // holds the 16-bit halves h = (r >> 3) & 1 of word kk of the chunks of rows (r & ~8) and
 // (r | 8), the lower row in the low half.  FP8 (one entry per MMA): the row's own chunk.
-// Rows past M read as 0x44444444 (position pair {0,1} in every group).  `rows` = M
-// rounded up to 16: a lane past M can still carry half of a real row's index.
+// Rows past M and slots past the index's (z >= slots, up to slots_out) read as
+// 0x44444444 (position pair {0,1} in every group).  `rows` (a multiple of 16 at
+// least M: a lane past M can still carry half of a real row's index) rows are
+// written per slot, 8 bytes each.
 constexpr int kMetaTile = 32;
 
-__global__ void __launch_bounds__(256) meta_native_kernel(const uint2* __restrict__ idx, uint4* __restrict__ native,
-                                                          int64_t M, int64_t rows, int64_t slots, int f16) {
+__global__ void __launch_bounds__(256) meta_native_kernel(const uint2* __restrict__ idx, uint2* __restrict__ native,
+                                                          int64_t M, int64_t rows, int64_t slots, int64_t slots_out,
+                                                          int f16) {
   griddep_launch_dependents();
   griddep_wait();   // launched with programmatic dependent launch
   __shared__ uint2 tile[kMetaTile][kMetaTile + 1];
-  const int64_t tiles_z = (slots + kMetaTile - 1) / kMetaTile;
+  const int64_t tiles_z = (slots_out + kMetaTile - 1) / kMetaTile;
   const int64_t tiles = tiles_z * ((rows + kMetaTile - 1) / kMetaTile);
   for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
     const int64_t r0 = (t / tiles_z) * kMetaTile;
@@ -314,8 +317,8 @@ __global__ void __launch_bounds__(256) meta_native_kernel(const uint2* __restric
     for (int i = threadIdx.x; i < kMetaTile * kMetaTile; i += blockDim.x) {
       const int zz = i / kMetaTile, rr = i % kMetaTile;
       const int64_t r = r0 + rr, z = z0 + zz;
-      if (r >= rows || z >= slots) continue;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r >= rows || z >= slots_out) continue;
+      uint2 v;
       if (f16) {
         const uint32_t sh = 16u * ((rr >> 3) & 1);
         const uint2 a = tile[rr & ~8][zz], b = tile[rr | 8][zz];
@@ -381,11 +384,10 @@ cudaError_t launch_splitk_reduce_i32(const int32_t* P, int ksplit, const int32_t
                     ksplit, n4, reinterpret_cast<const int4*>(C), reinterpret_cast<int4*>(D), clamp ? 1 : 0, fix);
 }
 
-cudaError_t launch_meta_native(const uint8_t* idx, void* native, int64_t M, int64_t K, bool f16, int bkl,
-                               int mmas, int num_sms, cudaStream_t stream) {
-  const int64_t slots = (K / bkl) * (f16 ? 1 : mmas);   // K / 64 in both layouts
-  const int64_t rows = (M + 15) / 16 * 16;
-  const int64_t tiles = ((slots + kMetaTile - 1) / kMetaTile) * ((rows + kMetaTile - 1) / kMetaTile);
+cudaError_t launch_meta_native(const uint8_t* idx, void* native, int64_t M, int64_t K, bool f16, int64_t rows,
+                               int64_t slots_out, int num_sms, cudaStream_t stream) {
+  const int64_t slots = K / 64;   // 8 index bytes per row each
+  const int64_t tiles = ((slots_out + kMetaTile - 1) / kMetaTile) * ((rows + kMetaTile - 1) / kMetaTile);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(tiles, int64_t(num_sms) * 8))), 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
@@ -395,8 +397,8 @@ cudaError_t launch_meta_native(const uint8_t* idx, void* native, int64_t M, int6
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, meta_native_kernel, reinterpret_cast<const uint2*>(idx), static_cast<uint4*>(native),
-                            M, rows, slots, f16 ? 1 : 0);
+  return cudaLaunchKernelEx(&cfg, meta_native_kernel, reinterpret_cast<const uint2*>(idx), static_cast<uint2*>(native),
+                            M, rows, slots, slots_out, f16 ? 1 : 0);
 }
 
 cudaError_t launch_i8_to_bf16(const void* a, bool a_unsigned, int a_offset, uint16_t* a16, int64_t na, const void* b,

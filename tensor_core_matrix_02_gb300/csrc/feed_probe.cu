@@ -89,8 +89,16 @@ __global__ void __launch_bounds__(kFeedThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- producer
-    const CUtensorMap* maps[4] = {&m0, &m1, &m2, &m3};
-    for (int b = 0; b < a.nbox; ++b) prefetch_tensormap(maps[b]);
+    // (the box loop is unrolled so that each map is named directly: a map picked
+    // through a runtime-indexed pointer would be copied to local memory and read
+    // from there by every copy, as the GEMM kernels never do)
+    int y[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const CUtensorMap* m = b == 0 ? &m0 : b == 1 ? &m1 : b == 2 ? &m2 : &m3;
+      if (b < a.nbox) prefetch_tensormap(m);
+      y[b] = b < a.nbox ? ((2 * cid + rank) * 128) % (a.height - a.rows[b] + 1) : 0;
+    }
     int stage = 0;
     uint32_t phase = 0;
     for (int it = 0; it < a.iters; ++it) {
@@ -98,10 +106,13 @@ __global__ void __launch_bounds__(kFeedThreads, 1)
       const uint32_t fb = mapa_shared(full_bar(stage), 0);
       if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2u * static_cast<uint32_t>(a.stage_bytes));
       const uint32_t dst = sbase + stage * a.stage_bytes;
-      for (int b = 0; b < a.nbox; ++b) {
-        const int x = static_cast<int>((static_cast<int64_t>(it) * a.row_bytes[b]) % kFeedRowBytes);
-        const int y = ((2 * cid + rank) * 128) % (a.height - a.rows[b] + 1);
-        tma_load_2d_pair(dst + a.smem_off[b], maps[b], x, y, fb);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const CUtensorMap* m = b == 0 ? &m0 : b == 1 ? &m1 : b == 2 ? &m2 : &m3;
+        if (b < a.nbox) {
+          const int x = (it * a.row_bytes[b]) & (kFeedRowBytes - 1);
+          tma_load_2d_pair(dst + a.smem_off[b], m, x, y[b], fb);
+        }
       }
       if (++stage == a.stages) { stage = 0; phase ^= 1u; }
     }

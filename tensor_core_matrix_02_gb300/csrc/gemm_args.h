@@ -30,6 +30,13 @@ struct GemmArgs {
   // tail_split K slices that write partials.  0: none.
   int tail_from = 0;
   int tail_split = 0;
+  // 4:2-sparse kernel: the index in its device-native layout, 8 bytes per row per 64
+  // logical K ([slot][row], meta_rows rows per slot)
+  const void* meta = nullptr;
+  int64_t meta_rows = 0;
+  // 4:2-sparse kernel, 16-bit B: the B map is the 3-D view (64 columns, K, N / 64
+  // chunks) and a stage's two column chunks come in one box
+  int b_chunks_3d = 0;
 };
 
 }  // namespace mma42

@@ -16,7 +16,9 @@ SparseInfo sparse_pair_info_of() {
   i.mmas = Cfg::MMAS;
   i.meta_slots = Cfg::META_SLOTS;
   i.b_atom_n = Cfg::B_ATOM_N;
+  i.b_chunks = Cfg::B_CHUNKS;
   i.b_rows_per_cta = Cfg::BKL;
+  i.epi_cols = Cfg::EPI_COLS;
   i.smem_bytes = Cfg::SMEM_BYTES;
   i.threads = Cfg::THREADS;
   return i;
@@ -62,7 +64,7 @@ cudaError_t sparse_pair_launch(const TensorMaps& m, const GemmArgs& args, int gr
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = cluster_config(grid, Cfg::THREADS, Cfg::SMEM_BYTES, 2, stream, attr);
-  return cudaLaunchKernelEx(&cfg, kernel, m.a, m.b, m.meta, m.c, m.d, args);
+  return cudaLaunchKernelEx(&cfg, kernel, m.a, m.b, m.c, m.d, args);
 }
 
 }  // namespace mma42

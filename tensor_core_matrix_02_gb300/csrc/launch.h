@@ -67,9 +67,11 @@ struct SparseInfo {
   int bka;              // compressed A elements per stage row (64 bytes)
   int bkl;              // logical K per stage
   int mmas;             // tcgen05.mma.sp per stage
-  int meta_slots;       // 128 x 16-byte index tiles per stage
+  int meta_slots;       // index slots (64 logical K each) per stage
   int b_atom_n;         // B box width (elements)
+  int b_chunks;         // b_atom_n-wide column chunks of B per CTA and stage
   int b_rows_per_cta;   // K rows of each B box
+  int epi_cols;         // f32 columns of the epilogue's C and D boxes (32: 128-byte rows, or 16)
   int smem_bytes;
   int threads;
 };
@@ -95,11 +97,13 @@ cudaError_t sparse_pair_f8_launch(const TensorMaps& m, const GemmArgs& a, int gr
 // the exact i8 variant of the kind::f16 kernel (bf16 operands, i32 chunk sums; C and D i32)
 int sparse_pair_i8_max_clusters();
 cudaError_t sparse_pair_i8_launch(const TensorMaps& m, const GemmArgs& a, int grid, cudaStream_t s);
-// Device-native index layout for the sparse GEMM (M rounded up to 16 rows): for slot
-// z = stage * mmas + kk and row r, 16 bytes holding the index word(s) TMEM lane r needs for MMA kk of that
-// stage (kind::f16 pairs rows r and r^8; FP8 uses each row's own 8 bytes).
-cudaError_t launch_meta_native(const uint8_t* idx, void* native, int64_t M, int64_t K, bool f16, int bkl,
-                               int mmas, int num_sms, cudaStream_t stream);
+// Device-native index layout for the sparse GEMM: slot z holds the index of logical K
+// [64 z, 64 z + 64); for each of `rows` rows (a multiple of 16, at least M), the 8
+// bytes TMEM lane r % 128 needs (kind::f16 pairs rows r and r^8, one 32-bit word per
+// 32-K MMA; FP8 uses each row's own 8 bytes).  Rows past M and slots from K / 64 up
+// to `slots_out` (a last stage that runs past K) hold positions {0, 1} everywhere.
+cudaError_t launch_meta_native(const uint8_t* idx, void* native, int64_t M, int64_t K, bool f16, int64_t rows,
+                               int64_t slots_out, int num_sms, cudaStream_t stream);
 
 // D = C + sum_s P[s]   (P: ksplit x M x N f32, fixed summation order); out: C and D
 // type, 0 f32, 1 f16, 2 bf16 (the f32 sum rounded to nearest even).

@@ -125,10 +125,10 @@ __global__ void __launch_bounds__(kPeakCtaThreads, 1)
           using Cfg = typename Sh::Cfg;
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
           if constexpr (SPARSE) {
-            const uint64_t ad = smem_desc(sa + kk * 32, 16, 8 * Cfg::A_ROW, LAYOUT_SW64);
+            const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, LAYOUT_SW128);
             const uint64_t bd = smem_desc(sb + kk * Cfg::B_KSTEP, Cfg::B_CHUNK_BYTES, 1024, LAYOUT_SW128);
-            const uint32_t mslot = (Cfg::META_SLOTS == 1) ? meta : meta + kk * Cfg::META_SLOT_COLS;
-            const uint32_t id = (Cfg::META_SLOTS == 1) ? (idesc | static_cast<uint32_t>(kk)) : idesc;
+            const uint32_t mslot = meta + (kk / Cfg::MMAS_PER_SLOT) * Cfg::META_SLOT_COLS;
+            const uint32_t id = idesc | static_cast<uint32_t>(kk % Cfg::MMAS_PER_SLOT);
             umma_sp_pair<KIND>(tmem_base, ad, bd, mslot, id, acc);
           } else {
             const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, LAYOUT_SW128);
