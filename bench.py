@@ -775,6 +775,46 @@ def run_aux(args):
                       "note": "inputs larger than L2 (>= 128 MB each); algorithmic bytes: read input, write output"}))
 
 
+# Stage shapes for the TMA feed probe: (label, [(rows, row bytes) per box], stages)
+FEED_STAGES = [
+    ("4:2 f16, 64-byte compressed-A rows, index box, two B chunks", [(128, 64), (8, 256), (64, 128), (64, 128)], 7),
+    ("4:2 FP8, 64-byte compressed-A rows, index box, one B chunk", [(128, 64), (16, 256), (128, 128)], 6),
+    ("dense bf16 (A, two B chunks)", [(128, 128), (64, 128), (64, 128)], 6),
+    ("dense FP8 (A, one B chunk)", [(128, 128), (128, 128)], 6),
+    ("4:2 f16, 128-byte rows, index box, two B chunks", [(128, 128), (16, 256), (128, 128), (128, 128)], 4),
+    ("4:2 FP8, 128-byte rows, index box, one B chunk", [(128, 128), (32, 256), (256, 128)], 3),
+    ("4:2 f16, 128-byte rows, B chunks in one box (index in registers)", [(128, 128), (256, 128)], 4),
+    ("4:2 FP8, 128-byte rows (index in registers)", [(128, 128), (256, 128)], 4),
+]
+
+
+def run_feed_probe(args):
+    """The TMA fill rate of a CTA pair's ring for the kernels' stage shapes and for
+    1-4 boxes of 64/128/256-byte rows: one JSON line per case."""
+    from tensor_core_matrix_02_gb300 import build, mma42 as mm
+    build.build()
+    torch.cuda.set_device(0)
+    cases = []
+    for src in (64 << 20, 1 << 30):
+        for label, boxes, st in FEED_STAGES:
+            for cl in (0, 19):
+                cases.append((label, boxes, st, cl, src))
+    for rows, rb in ((128, 64), (128, 128), (64, 128), (16, 256)):
+        for n in (1, 2, 3, 4):
+            boxes = [(rows, rb)] * n
+            sb = rows * rb * n
+            for kb in (96, 196):
+                cases.append((f"{n} x ({rows} rows x {rb} B)", boxes, max(2, min(16, kb * 1024 // sb)), 0, 64 << 20))
+    for label, boxes, st, cl, src in cases:
+        b, r = mm.mma_tma_feed_probe(boxes, st, clusters=cl, src_bytes=src)
+        sb = sum(x * y for x, y in boxes)
+        print(json.dumps({"stage": label, "boxes": boxes, "stages": st, "pairs": cl or "all", "source_mb": src >> 20,
+                          "stage_bytes": sb, "bytes_per_clk_sm": round(b, 2), "rows_per_clk_sm": round(r, 4),
+                          "clocks_per_stage": round(sb / b, 1)}), flush=True)
+    if mm.mma_sync_status() != 0:
+        raise RuntimeError("device error in the feed probe")
+
+
 def run_reference(args):
     """The oracle, as it stands, on the host cores; rank 0 only."""
     rank = int(os.environ.get("RANK", "0"))
@@ -819,6 +859,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=512, help="reference arm sample: every n-th row")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--feed-probe", action="store_true",
+                    help="TMA fill rate of the pair kernels' ring for their stage shapes (measurement helper)")
     ap.add_argument("--aux", action="store_true",
                     help="time only the bandwidth-bound steps (compression, pruning, quantisation)")
     ap.add_argument("--record-traffic", metavar="CSV", default=None,
@@ -834,6 +876,9 @@ def main():
         return
     if args.aux:
         run_aux(args)
+        return
+    if args.feed_probe:
+        run_feed_probe(args)
         return
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
