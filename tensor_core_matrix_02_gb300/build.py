@@ -23,7 +23,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 SOURCES = ["api.cu", "gemm_dense.cu", "gemm_pair.cu", "gemm_sparse_f16.cu", "gemm_sparse_f8.cu",
            "compress42.cu", "aux_kernels.cu", "noalloc.cu", "quantize.cu", "legacy_peak.cu",
-           "tc_peak.cu", "feed_probe.cu"]
+           "tc_peak.cu", "feed_probe.cu", "gemm_small.cu"]
 
 
 def _nvcc() -> str:

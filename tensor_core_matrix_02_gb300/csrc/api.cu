@@ -409,6 +409,64 @@ mma_status_t run_sparse(const DeviceState& ds, const void* vals, const uint8_t* 
   return from_cuda(e);
 }
 
+// Short K: the one-CTA-per-block kernel with all of a block's operands in flight at
+// once (gemm_small.cu), when K fits its shared memory and the blocks fit one wave.
+// MMA42_DENSE_KERNEL=small forces it whenever K fits; =single or =pair keep it out.
+bool use_small(const DeviceState& ds, int64_t M, int64_t N, int64_t K, bool f8) {
+  const SmallInfo si = small_info(f8);
+  if (K > static_cast<int64_t>(si.kb_max) * si.bk) return false;
+  if (const char* env = std::getenv("MMA42_DENSE_KERNEL")) {
+    if (std::strcmp(env, "small") == 0) return true;
+    if (std::strcmp(env, "single") == 0 || std::strcmp(env, "pair") == 0) return false;
+  }
+  const int64_t blocks = ((M + si.bm - 1) / si.bm) * ((N + si.bn - 1) / si.bn);
+  return blocks <= ds.num_sms;
+}
+
+mma_status_t run_small(const DeviceState& ds, bool f8, const void* A, int a_bytes, const void* B, int b_bytes,
+                       const void* C, void* D, int64_t M, int64_t N, int64_t K, uint32_t idesc, cudaStream_t stream) {
+  const SmallInfo si = small_info(f8);
+  GemmArgs a;
+  a.M = static_cast<int>(M);
+  a.N = static_cast<int>(N);
+  a.K = static_cast<int>(K);
+  a.tiles_m = static_cast<int>((M + si.bm - 1) / si.bm);
+  a.tiles_n = static_cast<int>((N + si.bn - 1) / si.bn);
+  a.kblocks = static_cast<int>((K + si.bk - 1) / si.bk);
+  a.ksplit = 1;
+  a.group_m = 1;
+  a.idesc = idesc;
+  a.err = ds.err;
+  a.wait_ns = g_wait_ns.load();
+  a.inject = 0;
+  TensorMaps m;
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+    const uint64_t str[1] = {static_cast<uint64_t>(K) * a_bytes};
+    const uint32_t box[2] = {static_cast<uint32_t>(si.bk), static_cast<uint32_t>(si.bm)};
+    if (!encode(&m.a, raw_type(a_bytes), 2, A, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MMA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(K)};
+    const uint64_t str[1] = {static_cast<uint64_t>(N) * b_bytes};
+    const uint32_t box[2] = {static_cast<uint32_t>(si.b_atom_n), static_cast<uint32_t>(si.bk)};
+    if (!encode(&m.b, raw_type(b_bytes), 2, B, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MMA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {static_cast<uint64_t>(N), static_cast<uint64_t>(M)};
+    const uint64_t str[1] = {static_cast<uint64_t>(N) * 4};
+    const uint32_t box[2] = {32u, 32u};
+    if (!encode(&m.c, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode(&m.d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, D, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MMA_ERR_CUDA;
+  }
+  m.meta = m.a;
+  m.p = m.d;
+  const cudaError_t e = launch_small(f8, m, a, stream);
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return from_cuda(e);
+}
+
 // The CTA-pair kernel (256 x 256 blocks) when there are enough blocks to give
 // every SM pair work, or when K is long enough that one wave of K slices (of at
 // least kMinSliceSteps k-steps) fills most pairs; otherwise the one-SM kernel.
@@ -935,6 +993,9 @@ mma_status_t mma_gemm_ex(const void* A, const void* B, const void* C, void* D, i
     return run_pair(*ds, t.acc == MMA_F16 ? V_PAIR_F16_OUTH : V_PAIR_BF16_OUTH, A, ea, B, eb, C, D, 2, M, N, K,
                     fmt_code(t.a), fmt_code(t.b), 0, s);
   const bool f8 = is_fp8(t.a);
+  if (use_small(*ds, M, N, K, f8))
+    return run_small(*ds, f8, A, ea, B, eb, C, D, M, N, K,
+                     make_idesc(fmt_code(t.a), fmt_code(t.b), 128, false, 128), s);
   if (use_pair(*ds, M, N, (K + (f8 ? 127 : 63)) / (f8 ? 128 : 64), true))
     return run_pair(*ds, f8 ? V_PAIR_F8 : V_PAIR_F16, A, ea, B, eb, C, D, 4, M, N, K, fmt_code(t.a),
                     fmt_code(t.b), 0, s);

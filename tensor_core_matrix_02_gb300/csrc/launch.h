@@ -134,6 +134,15 @@ int tc_peak_max_clusters(int kind);
 cudaError_t launch_tc_peak(int kind, int64_t iters, uint32_t idesc, uint64_t wait_ns, unsigned long long* cycles,
                            int* err, int clusters, cudaStream_t stream);
 
+// Short-K GEMM (gemm_small.cu): one CTA per 128 x 128 block, K at most kb_max * bk,
+// f32 C and D; C and D maps of 32 x 32 f32 boxes (128-byte swizzle), A of bk x 128,
+// B of b_atom_n x bk boxes.  Launched with programmatic dependent launch.
+struct SmallInfo {
+  int bm, bn, bk, b_atom_n, kb_max;
+};
+SmallInfo small_info(bool f8);
+cudaError_t launch_small(bool f8, const TensorMaps& m, const GemmArgs& a, cudaStream_t stream);
+
 // TMA feed probe (feed_probe.cu): the producer loop of the CTA-pair kernels alone.
 // Up to four boxes per stage (rows x row_bytes each, placed at smem_off within the
 // stage), `stages` stages of stage_bytes, iters stages per CTA; the maps are 2-D
