@@ -227,6 +227,35 @@ def algorithmic_bytes(p: W.Problem) -> int:
     return a + b + 2 * p.M * p.N * (2 if p.tacc in ("f16", "bf16") else 4)
 
 
+def graph_per_call(fn, calls: int = 200, reps: int = 5):
+    """Device time per call of `calls` back-to-back calls captured in one CUDA graph
+    (warm inputs; the host's per-call cost is out of the picture), median of `reps`
+    replays; (None, reason) if the calls cannot be captured."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn(); fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(calls):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(); g.replay(); b.record(); torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e3 / calls)
+        ts.sort()
+        return round(ts[len(ts) // 2], 3), f"{calls} calls in one CUDA graph, median of {reps} replays"
+    except Exception as e:   # a capture the driver refuses: report it, keep the run
+        torch.cuda.synchronize()
+        return None, f"not captured: {str(e).splitlines()[0][:120]}"
+
+
 def small_case(mm, dev, hbm_gbs: float, reps: int = 21) -> dict:
     """The smallest configuration (dense f16 128 x 128 x 256, one tile: launch- and
     latency-bound) timed per call on the device, warm (inputs in L2) and cold (L2
@@ -251,13 +280,15 @@ def small_case(mm, dev, hbm_gbs: float, reps: int = 21) -> dict:
             ts.append(a.elapsed_time(b) * 1e3)
         ts.sort()
         out[f"us_{mode}"] = round(ts[len(ts) // 2], 2)
+    out["us_per_call_in_graph"], out["graph_note"] = graph_per_call(lambda: mm.mma_gemm(p.A, p.B, p.C, D))
     byts = algorithmic_bytes(p)
     gbs = {m: byts / (out[f"us_{m}"] * 1e-6) / 1e9 for m in ("warm", "cold")}
     return {"workload": "dense_f16_128", "M": p.M, "N": p.N, "K": p.K, **out,
             "algorithmic_bytes": byts, "gbs_warm": round(gbs["warm"], 1), "gbs_cold": round(gbs["cold"], 1),
             "frac_of_hbm_warm": round(gbs["warm"] / hbm_gbs, 5), "frac_of_hbm_cold": round(gbs["cold"] / hbm_gbs, 5),
             "tflops_warm": round(p.flops / (out["us_warm"] * 1e-6) / 1e12, 3),
-            "what": "median of 21 single calls, each queued behind a device-side sleep"}
+            "what": "us_warm / us_cold: median of 21 single calls, each queued behind a device-side sleep "
+                    "(event times here move in steps of about 2 us); us_per_call_in_graph: back-to-back calls"}
 
 
 def record_traffic(args):

@@ -413,7 +413,7 @@ mma_status_t run_sparse(const DeviceState& ds, const void* vals, const uint8_t* 
 // once (gemm_small.cu), when K fits its shared memory and the blocks fit one wave.
 // MMA42_DENSE_KERNEL=small forces it whenever K fits; =single or =pair keep it out.
 bool use_small(const DeviceState& ds, int64_t M, int64_t N, int64_t K, bool f8) {
-  const SmallInfo si = small_info(f8);
+  const SmallInfo si = small_info(f8, false);
   if (K > static_cast<int64_t>(si.kb_max) * si.bk) return false;
   if (const char* env = std::getenv("MMA42_DENSE_KERNEL")) {
     if (std::strcmp(env, "small") == 0) return true;
@@ -423,9 +423,23 @@ bool use_small(const DeviceState& ds, int64_t M, int64_t N, int64_t K, bool f8) 
   return blocks <= ds.num_sms;
 }
 
+// Block width of the short-K kernel: 16-bit operands take 64-column blocks while
+// those still give at most one block per SM (each SM then loads and stores half as
+// much), otherwise 128.  MMA42_SMALL_BN=64|128 overrides the choice (tests).
+bool small_narrow(const DeviceState& ds, int64_t M, int64_t N, bool f8) {
+  if (f8) return false;
+  if (const char* env = std::getenv("MMA42_SMALL_BN")) {
+    if (std::strcmp(env, "64") == 0) return true;
+    if (std::strcmp(env, "128") == 0) return false;
+  }
+  return ((M + 127) / 128) * ((N + 63) / 64) <= ds.num_sms;
+}
+
 mma_status_t run_small(const DeviceState& ds, bool f8, const void* A, int a_bytes, const void* B, int b_bytes,
-                       const void* C, void* D, int64_t M, int64_t N, int64_t K, uint32_t idesc, cudaStream_t stream) {
-  const SmallInfo si = small_info(f8);
+                       const void* C, void* D, int64_t M, int64_t N, int64_t K, int a_fmt, int b_fmt,
+                       cudaStream_t stream) {
+  const SmallInfo si = small_info(f8, small_narrow(ds, M, N, f8));
+  const uint32_t idesc = make_idesc(a_fmt, b_fmt, si.bn, false, si.bm);
   GemmArgs a;
   a.M = static_cast<int>(M);
   a.N = static_cast<int>(N);
@@ -462,7 +476,7 @@ mma_status_t run_small(const DeviceState& ds, bool f8, const void* A, int a_byte
   }
   m.meta = m.a;
   m.p = m.d;
-  const cudaError_t e = launch_small(f8, m, a, stream);
+  const cudaError_t e = launch_small(f8, si.bn, m, a, stream);
   if (e == cudaSuccess) g_launches.fetch_add(1);
   return from_cuda(e);
 }
@@ -994,8 +1008,7 @@ mma_status_t mma_gemm_ex(const void* A, const void* B, const void* C, void* D, i
                     fmt_code(t.a), fmt_code(t.b), 0, s);
   const bool f8 = is_fp8(t.a);
   if (use_small(*ds, M, N, K, f8))
-    return run_small(*ds, f8, A, ea, B, eb, C, D, M, N, K,
-                     make_idesc(fmt_code(t.a), fmt_code(t.b), 128, false, 128), s);
+    return run_small(*ds, f8, A, ea, B, eb, C, D, M, N, K, fmt_code(t.a), fmt_code(t.b), s);
   if (use_pair(*ds, M, N, (K + (f8 ? 127 : 63)) / (f8 ? 128 : 64), true))
     return run_pair(*ds, f8 ? V_PAIR_F8 : V_PAIR_F16, A, ea, B, eb, C, D, 4, M, N, K, fmt_code(t.a),
                     fmt_code(t.b), 0, s);

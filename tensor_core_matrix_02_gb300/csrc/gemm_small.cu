@@ -1,5 +1,5 @@
-// gemm_small.cu -- D = A*B + C for short K: one CTA per 128 x 128 output block,
-// everything in flight at once.
+// gemm_small.cu -- D = A*B + C for short K: one CTA per 128 x 128 (or, for 16-bit
+// operands and few blocks, 128 x 64) output block, everything in flight at once.
 //
 // The operation is the matrix multiply-accumulate of "CDNA dense MFMA builtins",
 // section "Naming convention", over whole matrices, for K up to 4 k-blocks (256 for
@@ -8,9 +8,15 @@
 // scheduler, their ring's handshakes and a C load that waits for the accumulator.
 // Here one thread issues every A and B box (one barrier per k-block, so the MMAs of
 // a k-block start as it lands), each warp issues the C boxes of its own 32 rows at
-// the same time, one thread issues the MMAs (M = 128, N = 128) and commits once,
-// and each warp then adds C to its TMEM lanes in the C staging buffer and stores
-// its rows of D by TMA.  No ring, no persistent loop, 128 TMEM columns.
+// the same time, one thread issues the MMAs (M = 128, N = BN) and commits once,
+// and each warp then adds C to its TMEM lanes in the C staging buffer, box by box,
+// and stores each 32 x 32 box of D by TMA as soon as it is added.  No ring, no
+// persistent loop, BN TMEM columns.
+//
+// One SM takes in a k-block (A and B boxes) about every 540 SM clocks from L2, and
+// the block's loads, MMAs and epilogue run one after the other, so with few blocks
+// the 64-column form (16-bit operands) halves each SM's share: A is read by both
+// CTAs of a 128-row band, B, C and D are split between them.
 //
 // Every wait is bounded: a wait that runs out raises the device error word and the
 // abort flag; the MMA thread still commits, so TMEM is released only after the
@@ -25,10 +31,10 @@ namespace mma42 {
 
 namespace {
 
-template <int KIND>
+template <int KIND, int BN_>
 struct SmallCfg {
   static constexpr int BM = 128;
-  static constexpr int BN = 128;
+  static constexpr int BN = BN_;                          // 128, or 64 for 16-bit operands
   static constexpr int ELEM = (KIND == KIND_F16) ? 2 : 1;
   static constexpr int BK = 128 / ELEM;                   // K per box: one 128-byte row of A
   static constexpr int KB_MAX = 4;                        // k-blocks held at once
@@ -36,18 +42,20 @@ struct SmallCfg {
   static constexpr int MMAS = BK / UMMA_K;                // 4
   static constexpr int A_BYTES = BM * 128;                // 16 KB per k-block
   static constexpr int B_ATOM_N = 128 / ELEM;
-  static constexpr int B_CHUNKS = BN / B_ATOM_N;          // 2 (16-bit), 1 (FP8)
+  static constexpr int B_CHUNKS = BN / B_ATOM_N;          // 2 (16-bit, BN 128), 1 (FP8, or BN 64)
   static constexpr int B_CHUNK_BYTES = BK * 128;
-  static constexpr int B_BYTES = B_CHUNKS * B_CHUNK_BYTES;   // 16 KB per k-block
+  static constexpr int B_BYTES = B_CHUNKS * B_CHUNK_BYTES;   // 16 KB per k-block (8 KB at BN 64)
   static constexpr int B_KSTEP = UMMA_K * 128;
   static constexpr int KB_BYTES = A_BYTES + B_BYTES;
   static constexpr int C_BOX_BYTES = 32 * 32 * 4;         // 32 rows x 32 f32
-  static constexpr int C_BYTES = (BM / 32) * (BN / 32) * C_BOX_BYTES;   // 64 KB
+  static constexpr int NB = BN / 32;                      // C / D boxes per warp
+  static constexpr int C_BYTES = (BM / 32) * NB * C_BOX_BYTES;   // 64 KB (32 KB at BN 64)
   static constexpr int MISC_BYTES = 256;
   static constexpr int SMEM_BYTES = 1024 + KB_MAX * KB_BYTES + C_BYTES + MISC_BYTES;
   static constexpr int TMEM_COLS = BN;
   static constexpr int THREADS = 128;
   static_assert(KB_BYTES % 1024 == 0, "k-blocks keep 1024-byte alignment");
+  static_assert(B_CHUNKS >= 1 && BN % B_ATOM_N == 0, "B tile is whole 128-byte chunks");
   static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -58,12 +66,12 @@ __device__ __forceinline__ bool small_wait(uint32_t bar, uint32_t parity, const 
   return wait_phase(bar, parity, a, abort_flag);
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(SmallCfg<KIND>::THREADS, 1)
+template <int KIND, int BN>
+__global__ void __launch_bounds__(SmallCfg<KIND, BN>::THREADS, 1)
     gemm_small_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                       const GemmArgs args) {
-  using Cfg = SmallCfg<KIND>;
+  using Cfg = SmallCfg<KIND, BN>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -114,12 +122,13 @@ __global__ void __launch_bounds__(SmallCfg<KIND>::THREADS, 1)
   griddep_launch_dependents();
   griddep_wait();
   const uint32_t tmem_base = *tmem_slot;
-  // C of this warp's 32 rows: four 32 x 32 boxes, one barrier
-  const uint32_t cw = cbase + warp * 4 * Cfg::C_BOX_BYTES;
+  // C of this warp's 32 rows: NB boxes of 32 x 32, one barrier
+  const uint32_t cw = cbase + warp * Cfg::NB * Cfg::C_BOX_BYTES;
   if (lane == 0) {
-    mbar_arrive_expect_tx(c_bar(warp), 4 * Cfg::C_BOX_BYTES);
+    mbar_arrive_expect_tx(c_bar(warp), Cfg::NB * Cfg::C_BOX_BYTES);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tma_load_2d(cw + j * Cfg::C_BOX_BYTES, &tmC, n0 + 32 * j, m0 + 32 * warp, c_bar(warp));
+    for (int j = 0; j < Cfg::NB; ++j)
+      tma_load_2d(cw + j * Cfg::C_BOX_BYTES, &tmC, n0 + 32 * j, m0 + 32 * warp, c_bar(warp));
   }
   if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------- MMA issuer
@@ -140,11 +149,11 @@ __global__ void __launch_bounds__(SmallCfg<KIND>::THREADS, 1)
   // ----------------------------------------------------------- epilogue (all warps)
   const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
   bool ok = warp_wait_phase(acc_bar, 0, args, abort_flag) && !*abort_flag;
-  uint32_t R[128];
+  uint32_t R[BN];
   if (ok) {
     tc_fence_after();
 #pragma unroll
-    for (int j = 0; j < 4; ++j) tmem_ld_32x32b_x32_to(tmem_base + lane_off + j * 32, R + j * 32);
+    for (int j = 0; j < Cfg::NB; ++j) tmem_ld_32x32b_x32_to(tmem_base + lane_off + j * 32, R + j * 32);
     tmem_wait_ld();
   }
   tc_fence_before();
@@ -152,24 +161,28 @@ __global__ void __launch_bounds__(SmallCfg<KIND>::THREADS, 1)
   if (ok) {
     uint8_t* rows = smem + (cw - sbase) + lane * 128;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < Cfg::NB; ++j) {
+      // a box's eight 16-byte chunks of C are all loaded before any sum is stored
+      // back (loads issued after a store to the same buffer would wait for it)
+      uint8_t* box = rows + j * Cfg::C_BOX_BYTES;
+      uint4 cv[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) cv[c] = *reinterpret_cast<const uint4*>(box + ((c ^ (lane & 7)) << 4));
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        uint4* p = reinterpret_cast<uint4*>(rows + j * Cfg::C_BOX_BYTES + ((c ^ (lane & 7)) << 4));
-        const uint4 cv = *p;
         uint4 v;
-        v.x = __float_as_uint(__uint_as_float(cv.x) + __uint_as_float(R[j * 32 + 4 * c + 0]));
-        v.y = __float_as_uint(__uint_as_float(cv.y) + __uint_as_float(R[j * 32 + 4 * c + 1]));
-        v.z = __float_as_uint(__uint_as_float(cv.z) + __uint_as_float(R[j * 32 + 4 * c + 2]));
-        v.w = __float_as_uint(__uint_as_float(cv.w) + __uint_as_float(R[j * 32 + 4 * c + 3]));
-        *p = v;
+        v.x = __float_as_uint(__uint_as_float(cv[c].x) + __uint_as_float(R[j * 32 + 4 * c + 0]));
+        v.y = __float_as_uint(__uint_as_float(cv[c].y) + __uint_as_float(R[j * 32 + 4 * c + 1]));
+        v.z = __float_as_uint(__uint_as_float(cv[c].z) + __uint_as_float(R[j * 32 + 4 * c + 2]));
+        v.w = __float_as_uint(__uint_as_float(cv[c].w) + __uint_as_float(R[j * 32 + 4 * c + 3]));
+        *reinterpret_cast<uint4*>(box + ((c ^ (lane & 7)) << 4)) = v;
       }
+      // the box of D leaves while the next one is added
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tma_store_2d(&tmD, n0 + 32 * j, m0 + 32 * warp, cw + j * Cfg::C_BOX_BYTES);
     }
-    fence_proxy_async_smem();
-    __syncwarp();
     if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tma_store_2d(&tmD, n0 + 32 * j, m0 + 32 * warp, cw + j * Cfg::C_BOX_BYTES);
       bulk_commit();
       bulk_wait_read_all();
     }
@@ -185,10 +198,10 @@ __global__ void __launch_bounds__(SmallCfg<KIND>::THREADS, 1)
   }
 }
 
-template <int KIND>
+template <int KIND, int BN>
 cudaError_t launch_small_kind(const TensorMaps& m, const GemmArgs& a, cudaStream_t stream) {
-  using Cfg = SmallCfg<KIND>;
-  auto kernel = gemm_small_kernel<KIND>;
+  using Cfg = SmallCfg<KIND, BN>;
+  auto kernel = gemm_small_kernel<KIND, BN>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, a.tiles_m * a.tiles_n, Cfg::THREADS, Cfg::SMEM_BYTES, stream, m.a, m.b, m.c, m.d, a);
@@ -196,24 +209,27 @@ cudaError_t launch_small_kind(const TensorMaps& m, const GemmArgs& a, cudaStream
 
 }  // namespace
 
-SmallInfo small_info(bool f8) {
+SmallInfo small_info(bool f8, bool narrow) {
   SmallInfo i;
   if (f8) {
-    i.bk = SmallCfg<KIND_F8>::BK;
-    i.b_atom_n = SmallCfg<KIND_F8>::B_ATOM_N;
-    i.kb_max = SmallCfg<KIND_F8>::KB_MAX;
+    i.bk = SmallCfg<KIND_F8, 128>::BK;
+    i.b_atom_n = SmallCfg<KIND_F8, 128>::B_ATOM_N;
+    i.kb_max = SmallCfg<KIND_F8, 128>::KB_MAX;
+    i.bn = 128;
   } else {
-    i.bk = SmallCfg<KIND_F16>::BK;
-    i.b_atom_n = SmallCfg<KIND_F16>::B_ATOM_N;
-    i.kb_max = SmallCfg<KIND_F16>::KB_MAX;
+    i.bk = SmallCfg<KIND_F16, 128>::BK;
+    i.b_atom_n = SmallCfg<KIND_F16, 128>::B_ATOM_N;
+    i.kb_max = SmallCfg<KIND_F16, 128>::KB_MAX;
+    i.bn = narrow ? 64 : 128;
   }
   i.bm = 128;
-  i.bn = 128;
   return i;
 }
 
-cudaError_t launch_small(bool f8, const TensorMaps& m, const GemmArgs& a, cudaStream_t stream) {
-  return f8 ? launch_small_kind<KIND_F8>(m, a, stream) : launch_small_kind<KIND_F16>(m, a, stream);
+cudaError_t launch_small(bool f8, int bn, const TensorMaps& m, const GemmArgs& a, cudaStream_t stream) {
+  if (f8) return bn == 128 ? launch_small_kind<KIND_F8, 128>(m, a, stream) : cudaErrorInvalidValue;
+  if (bn == 64) return launch_small_kind<KIND_F16, 64>(m, a, stream);
+  return bn == 128 ? launch_small_kind<KIND_F16, 128>(m, a, stream) : cudaErrorInvalidValue;
 }
 
 }  // namespace mma42

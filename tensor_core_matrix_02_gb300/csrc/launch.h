@@ -140,8 +140,10 @@ cudaError_t launch_tc_peak(int kind, int64_t iters, uint32_t idesc, uint64_t wai
 struct SmallInfo {
   int bm, bn, bk, b_atom_n, kb_max;
 };
-SmallInfo small_info(bool f8);
-cudaError_t launch_small(bool f8, const TensorMaps& m, const GemmArgs& a, cudaStream_t stream);
+// `narrow`: 64-column blocks (16-bit operands only; FP8 blocks stay 128 wide).
+SmallInfo small_info(bool f8, bool narrow);
+// bn: 128, or 64 for 16-bit operands; anything else is cudaErrorInvalidValue.
+cudaError_t launch_small(bool f8, int bn, const TensorMaps& m, const GemmArgs& a, cudaStream_t stream);
 
 // TMA feed probe (feed_probe.cu): the producer loop of the CTA-pair kernels alone.
 // Up to four boxes per stage (rows x row_bytes each, placed at smem_off within the
