@@ -20,7 +20,8 @@
 //
 // Every wait is bounded: a wait that runs out raises the device error word and the
 // abort flag; the MMA thread still commits, so TMEM is released only after the
-// MMAs it issued have completed, and D is not stored.
+// MMAs it issued have completed, D is not stored, and the loads already issued land
+// before the block exits.
 #include <cstdint>
 
 #include "gemm_kernel.cuh"
@@ -189,6 +190,11 @@ __global__ void __launch_bounds__(SmallCfg<KIND, BN>::THREADS, 1)
   } else if (lane == 0) {
     // the C loads were issued: let them land before the block's memory is released
     drain_wait(c_bar(warp), 0, args.wait_ns);
+  }
+  // after an abort, the A and B loads still in flight land before the block's
+  // shared memory is released
+  if (threadIdx.x == 0 && *abort_flag) {
+    for (int kb = 0; kb < kbs; ++kb) drain_wait(kb_bar(kb), 0, args.wait_ns);
   }
   __syncwarp();
   __syncthreads();

@@ -209,11 +209,12 @@ def test_dense_each_kernel_matches_oracle(oracle, monkeypatch, kernel, kind, M, 
 
 
 # the short-K kernel (one CTA per 128 x 128 block, or 128 x 64 for 16-bit operands,
-# all of a block's operands in flight at once): its longest K (4 k-blocks), a ragged
-# K, several ragged blocks, and in place, at both block widths
+# all of a block's operands in flight at once): 1, 2 and 4 k-blocks, a ragged K,
+# several ragged blocks, and in place, at both block widths
 @pytest.mark.parametrize("bn", ["64", "128"])
 @pytest.mark.parametrize("kind", ["f16", "bf16", "e4m3xe5m2", "e5m2xe4m3"])
-@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (1000, 704, 208), (1000, 704, 512), (33, 48, 16)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 256), (1000, 704, 208), (1000, 704, 512), (33, 48, 16),
+                                   (256, 320, 128), (200, 144, 64)])
 def test_small_kernel_matches_oracle(oracle, monkeypatch, kind, M, N, K, bn):
     if bn == "64" and kind.startswith("e"):
         pytest.skip("FP8 blocks are 128 columns wide (one 128-byte row of B)")
