@@ -282,7 +282,9 @@ mma_status_t mma_tma_feed_probe(int32_t nbox, const int32_t* box_rows, const int
  * pipeline stage but never issues that stage's loads.  `mode` 2: the next launch
  * of a CTA-pair kernel (dense mma_gemm on the pair kernel, or sparse42_gemm) has
  * its first cluster arm its first stage for 16 bytes more than that stage's loads
- * bring (every load is issued and lands).  Either way that stage never completes,
+ * bring (every load is issued and lands).  `mode` 3: the next launch of the short-K
+ * kernel (mma_gemm with K of at most four k-blocks) has its first block arm its
+ * first k-block for 16 bytes more than its loads bring.  Either way that stage never completes,
  * the MMA thread's bounded wait runs out and the timeout path is exercised
  * (MMA_ERR_TIMEOUT from mma_sync_status).  The hook disarms itself when a launch
  * of its kind takes it; 0 disarms it. */

@@ -452,7 +452,7 @@ mma_status_t run_small(const DeviceState& ds, bool f8, const void* A, int a_byte
   a.idesc = idesc;
   a.err = ds.err;
   a.wait_ns = g_wait_ns.load();
-  a.inject = 0;
+  a.inject = take_inject(3);
   TensorMaps m;
   {
     const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};

@@ -105,7 +105,11 @@ __global__ void __launch_bounds__(SmallCfg<KIND, BN>::THREADS, 1)
     griddep_wait();
     for (int kb = 0; kb < kbs; ++kb) {
       const uint32_t sa = sbase + kb * Cfg::KB_BYTES;
-      mbar_arrive_expect_tx(kb_bar(kb), Cfg::KB_BYTES);
+      // test hook (mma_debug_inject(3)): block 0 arms its first k-block for 16 bytes
+      // more than its loads bring, so that barrier never completes and the MMA
+      // thread's bounded wait runs out; every load is still issued and lands
+      const uint32_t extra = (args.inject == 3 && blockIdx.x == 0 && kb == 0) ? 16u : 0u;
+      mbar_arrive_expect_tx(kb_bar(kb), Cfg::KB_BYTES + extra);
       tma_load_2d(sa, &tmA, kb * Cfg::BK, m0, kb_bar(kb));
 #pragma unroll
       for (int c = 0; c < Cfg::B_CHUNKS; ++c)

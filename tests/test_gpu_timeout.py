@@ -4,7 +4,8 @@ The test hook mma_debug_inject(1) makes the next one-SM dense launch arm its
 first pipeline stage without issuing that stage's loads; mma_debug_inject(2)
 makes the next CTA-pair launch (dense or 4:2-sparse) arm its first cluster's
 first stage for 16 bytes more than its loads bring, every load still issued and
-landing.  Either way the MMA thread's bounded wait on that stage runs out.
+landing; mma_debug_inject(3) does the same to the short-K kernel's first k-block.
+Either way the MMA thread's bounded wait on that stage runs out.
 Nothing faults or hangs: the kernel records MMA_ERR_TIMEOUT in the device error
 word, the roles of the CTA (and, in a pair, the peer CTA's own bounded waits)
 stop, issued copies are drained, TMEM is freed and the kernel returns.  The
@@ -42,11 +43,11 @@ def test_wait_timeout_reported_then_next_call_correct(oracle):
     assert_matches(D, oracle_dense(oracle, p), "bf16", "after timeout")
 
 
-def _timeout_then(lib, call):
+def _timeout_then(lib, call, mode=2):
     assert mma42.mma_sync_status() == 0
     lib.mma_set_wait_limit_ns(50_000_000)          # 50 ms
     try:
-        lib.mma_debug_inject(2)
+        lib.mma_debug_inject(mode)
         call()
         status = mma42.mma_sync_status()
     finally:
@@ -78,3 +79,16 @@ def test_sparse_kernel_wait_timeout_then_next_call_correct(oracle, name):
     ov, oi, _ = oracle.compress(W.bits(p.A), p.ta)
     ref = ref_sparse(oracle, ov, oi, p.ta, W.bits(p.B), p.tb, p.C.numpy(), p.K)
     assert_matches(D, ref, p.ta, f"{name} after timeout")
+
+
+@pytest.mark.parametrize("name,bn", [("dense_f16_128", "64"), ("dense_f16_128", "128"), ("dense_e4m3_16384", "128")])
+def test_small_kernel_wait_timeout_then_next_call_correct(oracle, monkeypatch, name, bn):
+    """The short-K kernel's first block gives up on its first k-block; the block's
+    issued loads land before it exits, and the next call is correct."""
+    monkeypatch.setenv("MMA42_DENSE_KERNEL", "small")
+    monkeypatch.setenv("MMA42_SMALL_BN", bn)
+    lib = mma42.load_library()
+    p = W.make(name, M=256, N=384, K=256)
+    A, B, C = p.A.cuda(), p.B.cuda(), p.C.cuda()
+    _timeout_then(lib, lambda: mma42.mma_gemm(A, B, C), mode=3)
+    assert_matches(gpu_dense(p), oracle_dense(oracle, p), p.ta, f"{name} short-K kernel after timeout")
