@@ -74,11 +74,11 @@ struct PairCfg {
   static constexpr int A_BYTES = BM * 128;                // 16 KB
   static constexpr int B_ATOM_N = 128 / ELEM;
   static constexpr int B_COLS = BN / 2;                   // columns of B staged by one CTA
-  static constexpr int B_CHUNKS = B_COLS / B_ATOM_N;      // 2 (16-bit), 1 (FP8, or INTACC)
+  static constexpr int B_CHUNKS = B_COLS / B_ATOM_N;      // 2 (16-bit, INTACC too), 1 (FP8)
   static constexpr int B_CHUNK_BYTES = BK * 128;
-  static constexpr int B_BYTES = B_CHUNKS * B_CHUNK_BYTES;   // 16 KB (8 KB INTACC)
+  static constexpr int B_BYTES = B_CHUNKS * B_CHUNK_BYTES;   // 16 KB
   static constexpr int B_KSTEP = UMMA_K * 128;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA (24 KB INTACC)
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB per CTA
   static constexpr int EPI_WARPS = 8;
   static constexpr int EPI_BUF_BYTES = 32 * 32 * 4;
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_BUF_BYTES;
