@@ -86,7 +86,9 @@ struct SparsePairCfg {
   // instruction on sm_103a) gives each MMA its own slot, 64 bits in two columns.
   static constexpr int MMAS_PER_SLOT = (KIND == KIND_F16) ? 2 : 1;
   static constexpr int META_SLOTS = MMAS / MMAS_PER_SLOT;    // per stage: 2 (f16), 4 (FP8)
-  static constexpr int META_SLOT_BYTES = BM * 16;         // one slot as a 128 x 16-byte tile (tcgen05.cp form)
+  // one stage's index as 128 x 16-byte tiles: the form the tcgen05 peak measurement
+  // copies into TMEM with tcgen05.cp (the GEMM's index writers use tcgen05.st)
+  static constexpr int META_SLOT_BYTES = BM * 16;
   static constexpr int META_BYTES = META_SLOTS * META_SLOT_BYTES;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 48 KB
   static constexpr int EPI_WARPS = 8;
