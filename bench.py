@@ -295,23 +295,14 @@ def record_traffic(args):
     """Read an ncu CSV (--metrics dram__bytes_read.sum,dram__bytes_write.sum,
     gpu__time_duration.sum) of one workload's GEMM launches and store the DRAM
     bytes per launch, with the digest of the kernel's sources, in traffic.json."""
-    import csv
     if not args.workloads or len(args.workloads) != 1:
         raise SystemExit("--record-traffic needs exactly one --workloads entry")
     name = args.workloads[0]
     r = W.RECIPES[name]
     prob = W.Problem(name, r.M, r.N, r.K, r.ta, r.tb, r.tacc, None, None, None, r.sparse, None)
     kernel, pattern = kernel_of(prob)
-    with open(args.record_traffic) as f:
-        rows = [ln for ln in f if ln.startswith('"')]
-    launches = {}
-    for row in csv.DictReader(rows):
-        if pattern not in row["Kernel Name"]:
-            continue
-        m = launches.setdefault(row["ID"], {})
-        m[row["Metric Name"]] = float(row["Metric Value"].replace(",", ""))
     need = ("dram__bytes_read.sum", "dram__bytes_write.sum")
-    got = [m for m in launches.values() if all(k in m for k in need)]
+    got = [m for m in _ncu_launches(args.record_traffic, pattern) if all(k in m for k in need)]
     if not got:
         raise SystemExit(f"no {pattern} launch with DRAM counters in {args.record_traffic}")
     rd = sum(m["dram__bytes_read.sum"] for m in got) / len(got)
@@ -340,9 +331,19 @@ NCU_METRICS = ("gpu__time_duration.sum", "dram__bytes_read.sum", "dram__bytes_wr
                "gpu__dram_throughput.avg.pct_of_peak_sustained_elapsed", "sm__cycles_elapsed.avg.per_second")
 
 
+# ncu prints a metric in the unit its "Metric Unit" column names, scaled by magnitude
+# in some outputs (SI prefixes): values are brought to bytes, nanoseconds and hertz
+NCU_UNIT_SCALE = {"byte": 1.0, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12,
+                  "ns": 1.0, "nsecond": 1.0, "us": 1e3, "usecond": 1e3, "ms": 1e6, "msecond": 1e6,
+                  "s": 1e9, "second": 1e9,
+                  "hz": 1.0, "khz": 1e3, "mhz": 1e6, "ghz": 1e9,
+                  "%": 1.0, "": 1.0}
+
+
 def _ncu_launches(csv_path: str, pattern: str) -> list[dict]:
     """Per-launch metric dictionaries of the kernels matching ``pattern`` in an ncu
-    CSV (``--csv`` output of ``--metrics``)."""
+    CSV (``--csv`` output of ``--metrics``), in base units (an unknown unit is an
+    error, not a silent misreading)."""
     import csv
     with open(csv_path) as f:
         rows = [ln for ln in f if ln.startswith('"')]
@@ -352,9 +353,13 @@ def _ncu_launches(csv_path: str, pattern: str) -> list[dict]:
             continue
         m = launches.setdefault(row["ID"], {})
         try:
-            m[row["Metric Name"]] = float(row["Metric Value"].replace(",", ""))
+            v = float(row["Metric Value"].replace(",", ""))
         except ValueError:
-            pass
+            continue
+        unit = row.get("Metric Unit", "").strip().lower()
+        if unit not in NCU_UNIT_SCALE:
+            raise SystemExit(f"{csv_path}: {row['Metric Name']} in unknown unit {unit!r}")
+        m[row["Metric Name"]] = v * NCU_UNIT_SCALE[unit]
     return list(launches.values())
 
 
