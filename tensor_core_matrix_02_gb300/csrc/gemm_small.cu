@@ -195,9 +195,11 @@ __global__ void __launch_bounds__(SmallCfg<KIND, BN>::THREADS, 1)
     // the C loads were issued: let them land before the block's memory is released
     drain_wait(c_bar(warp), 0, args.wait_ns);
   }
-  // after an abort, the A and B loads still in flight land before the block's
-  // shared memory is released
-  if (threadIdx.x == 0 && *abort_flag) {
+  // the A and B loads land before the block's shared memory is released: after a
+  // normal run every k-block's barrier has completed (the MMA thread waited on each
+  // before its commit) and these waits return at once; after an abort they cover
+  // the loads still in flight, whichever thread gave up
+  if (threadIdx.x == 0) {
     for (int kb = 0; kb < kbs; ++kb) drain_wait(kb_bar(kb), 0, args.wait_ns);
   }
   __syncwarp();
